@@ -1,0 +1,1054 @@
+// libgpt_b300: runtime and C ABI for KV-cached GPT-2 generation on sm_103a.
+//
+// One model = library-owned weights (nn.Linear layout), a contiguous KV cache
+// [layer][k|v][batch][head][position][64], activation buffers sized for max_batch x
+// block_size tokens, a device error word and a device-resident cache length.
+//
+// A forward pass over B x T new tokens (prefill: T = prompt length from an empty cache;
+// decode: T = 1 at position = cache length) enqueues:
+//   embed -> per layer [ln_1 -> c_attn GEMM (+ KV append) -> attention -> c_proj GEMM
+//   (+ residual) -> ln_2 -> c_fc GEMM (+ GELU) -> mlp c_proj GEMM (+ residual)] ->
+//   ln_f on each sequence's last position -> lm_head GEMM (tied wte) -> fp32 logits
+// ("nanoGPT 架构分析", wangbinyq.github.io, §4.1; "原生 nanoGPT 模型服务首选", §"一个值得做的改进").
+// gpt_generate captures one decode step plus its draw as a CUDA graph and replays it.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/gpt.h"
+#include "attention.cuh"
+#include "common.cuh"
+#include "gemm.cuh"
+#include "norm.cuh"
+#include "sampler.cuh"
+
+using namespace kvgpt;
+using bf16 = __nv_bfloat16;
+
+namespace {
+
+thread_local std::string g_detail;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_detail = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return e == cudaErrorMemoryAllocation ? GPT_ENOMEM : GPT_ECUDA;
+}
+
+#define CK(call)                                                        \
+  do {                                                                  \
+    cudaError_t e_ = (call);                                            \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);                 \
+  } while (0)
+
+inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// ------------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Row-major bf16 matrix [rows][cols] read in boxes of box_rows x 64 with 128-byte swizzle.
+int make_tmap(CUtensorMap* map, const void* ptr, long long rows, long long cols, int box_rows) {
+  if (!load_encode()) {
+    g_detail = "cuTensorMapEncodeTiled unavailable";
+    return GPT_EUNSUPPORTED;
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(TC_BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_detail = "cuTensorMapEncodeTiled failed (" + std::to_string(static_cast<int>(r)) + ")";
+    return GPT_ECUDA;
+  }
+  return GPT_OK;
+}
+
+// ------------------------------------------------------------------ GEMM launch
+
+unsigned long long g_attr_mask[64] = {};  // per kernel slot: devices whose smem attribute is set
+std::mutex g_attr_mu;
+
+constexpr int TC_STAGES = 4;
+
+template <int BN, bool HILO, int EPI>
+cudaError_t attr_tc(int slot, int dev) {
+  using S = TcSmem<BN, TC_STAGES, HILO>;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (!(g_attr_mask[slot] & (1ull << dev))) {
+    cudaError_t r = cudaFuncSetAttribute(gemm_tc_kernel<BN, TC_STAGES, HILO, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+    if (r != cudaSuccess) return r;
+    g_attr_mask[slot] |= 1ull << dev;
+  }
+  return cudaSuccess;
+}
+
+template <int BN, bool HILO, int EPI>
+cudaError_t launch_tc(int slot, int dev, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                      int splits, const Epi<bf16>& e, cudaStream_t st) {
+  constexpr int STAGES = TC_STAGES;
+  using S = TcSmem<BN, STAGES, HILO>;
+  auto kern = gemm_tc_kernel<BN, STAGES, HILO, EPI>;
+  cudaError_t r = attr_tc<BN, HILO, EPI>(slot, dev);
+  if (r != cudaSuccess) return r;
+  const int kb = K / TC_BK;
+  const int kbps = cdiv(kb, splits);
+  dim3 grid(cdiv(N, BN), cdiv(M, TC_BM), splits);
+  kern<<<grid, TC_THREADS, S::TOTAL, st>>>(ta, tb, kb, kbps, e);
+  return cudaGetLastError();
+}
+
+cudaError_t dispatch_tc(int bn, bool hilo, int epi, int dev, const CUtensorMap& ta, const CUtensorMap& tb, int M,
+                        int N, int K, int splits, const Epi<bf16>& e, cudaStream_t st) {
+#define KVGPT_TC_CASE(BN, H, E, SLOT) \
+  if (bn == BN && hilo == H && epi == E) return launch_tc<BN, H, E>(SLOT, dev, ta, tb, M, N, K, splits, e, st);
+  KVGPT_TC_CASE(64, false, EPI_F32, 0)
+  KVGPT_TC_CASE(64, false, EPI_RESID, 1)
+  KVGPT_TC_CASE(64, false, EPI_GELU, 2)
+  KVGPT_TC_CASE(64, false, EPI_QKV, 3)
+  KVGPT_TC_CASE(64, true, EPI_F32, 4)
+  KVGPT_TC_CASE(64, true, EPI_RESID, 5)
+  KVGPT_TC_CASE(64, true, EPI_GELU, 6)
+  KVGPT_TC_CASE(64, true, EPI_QKV, 7)
+  KVGPT_TC_CASE(128, false, EPI_F32, 8)
+  KVGPT_TC_CASE(128, false, EPI_RESID, 9)
+  KVGPT_TC_CASE(128, false, EPI_GELU, 10)
+  KVGPT_TC_CASE(128, false, EPI_QKV, 11)
+  KVGPT_TC_CASE(128, true, EPI_F32, 12)
+  KVGPT_TC_CASE(128, true, EPI_RESID, 13)
+  KVGPT_TC_CASE(128, true, EPI_GELU, 14)
+  KVGPT_TC_CASE(128, true, EPI_QKV, 15)
+  KVGPT_TC_CASE(256, false, EPI_F32, 16)
+  KVGPT_TC_CASE(256, false, EPI_RESID, 17)
+  KVGPT_TC_CASE(256, false, EPI_GELU, 18)
+  KVGPT_TC_CASE(256, false, EPI_QKV, 19)
+#undef KVGPT_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t set_tc_attr(int bn, bool hilo, int epi, int dev) {
+#define KVGPT_TC_ATTR(BN, H, E, SLOT) \
+  if (bn == BN && hilo == H && epi == E) return attr_tc<BN, H, E>(SLOT, dev);
+  KVGPT_TC_ATTR(64, false, EPI_F32, 0)
+  KVGPT_TC_ATTR(64, false, EPI_RESID, 1)
+  KVGPT_TC_ATTR(64, false, EPI_GELU, 2)
+  KVGPT_TC_ATTR(64, false, EPI_QKV, 3)
+  KVGPT_TC_ATTR(64, true, EPI_F32, 4)
+  KVGPT_TC_ATTR(64, true, EPI_RESID, 5)
+  KVGPT_TC_ATTR(64, true, EPI_GELU, 6)
+  KVGPT_TC_ATTR(64, true, EPI_QKV, 7)
+  KVGPT_TC_ATTR(128, false, EPI_F32, 8)
+  KVGPT_TC_ATTR(128, false, EPI_RESID, 9)
+  KVGPT_TC_ATTR(128, false, EPI_GELU, 10)
+  KVGPT_TC_ATTR(128, false, EPI_QKV, 11)
+  KVGPT_TC_ATTR(128, true, EPI_F32, 12)
+  KVGPT_TC_ATTR(128, true, EPI_RESID, 13)
+  KVGPT_TC_ATTR(128, true, EPI_GELU, 14)
+  KVGPT_TC_ATTR(128, true, EPI_QKV, 15)
+  KVGPT_TC_ATTR(256, false, EPI_F32, 16)
+  KVGPT_TC_ATTR(256, false, EPI_RESID, 17)
+  KVGPT_TC_ATTR(256, false, EPI_GELU, 18)
+  KVGPT_TC_ATTR(256, false, EPI_QKV, 19)
+#undef KVGPT_TC_ATTR
+  return cudaErrorInvalidValue;
+}
+
+// Raise the dynamic shared memory limit of every tensor-core GEMM instantiation and of
+// the sampler once per device, before any stream capture can need them.
+cudaError_t init_kernel_attrs(int dev) {
+  static const int bns[3] = {64, 128, 256};
+  for (int bi = 0; bi < 3; ++bi)
+    for (int h = 0; h < 2; ++h)
+      for (int epi = 0; epi < 4; ++epi) {
+        if (bns[bi] == 256 && h) continue;
+        cudaError_t r = set_tc_attr(bns[bi], h != 0, epi, dev);
+        if (r != cudaSuccess) return r;
+      }
+  return cudaSuccess;
+}
+
+struct GemmPlan {
+  int bn = 64;
+  int splits = 1;
+};
+
+// Output tile width and split-K count: wide tiles when there are enough tiles to fill the
+// GPU, otherwise 64-wide tiles with the K range split until about one wave of CTAs.
+GemmPlan plan_gemm(int M, int N, int K, int num_sms, bool hilo, size_t ws_bytes) {
+  GemmPlan p;
+  const int mt = cdiv(M, TC_BM), kb = K / TC_BK;
+  if (!hilo && N % 256 == 0 && mt * (N / 256) >= num_sms) {
+    p.bn = 256;
+  } else if (N % 128 == 0 && mt * (N / 128) >= num_sms) {
+    p.bn = 128;
+  } else {
+    p.bn = 64;
+    if (N % 16 == 0) {
+      const int tiles = mt * cdiv(N, 64);
+      int s = std::max(1, std::min(kb, num_sms / std::max(1, tiles)));
+      while (s > 1 && static_cast<size_t>(s) * M * N * sizeof(float) > ws_bytes) --s;
+      const int kbps = cdiv(kb, s);
+      p.splits = cdiv(kb, kbps);
+    }
+  }
+  return p;
+}
+
+// ------------------------------------------------------------------ small kernels
+
+__global__ void set_ints_kernel(int* a, int va, int* b, int vb) {
+  if (a) *a = va;
+  if (b) *b = vb;
+}
+__global__ void advance_kernel(int* pos, int* step) {
+  *pos += 1;
+  *step += 1;
+}
+
+int map_error_word(int w) {
+  if (w & ERR_TOKEN) return GPT_ETOKEN;
+  if (w & ERR_TIMEOUT) return GPT_ETIMEOUT;
+  if (w & ERR_POSITION) return GPT_EPOSITION;
+  return GPT_OK;
+}
+
+cudaError_t set_sampler_smem(int dev, int V) {
+  static int done_bytes[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  const int bytes = V * static_cast<int>(sizeof(float));
+  if (done_bytes[dev] >= bytes) return cudaSuccess;
+  cudaError_t r = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (r == cudaSuccess) done_bytes[dev] = bytes;
+  return r;
+}
+
+constexpr int MAX_VOCAB = 57344;
+
+// ------------------------------------------------------------------ stand-alone op scratch
+
+struct OpCtx {
+  int* err = nullptr;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  unsigned int* tickets = nullptr;
+  size_t n_tickets = 0;
+};
+OpCtx g_op[64];
+std::mutex g_op_mu;
+
+int op_ctx(OpCtx** out, size_t ws_need, size_t tickets_need) {
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return GPT_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_op_mu);
+  OpCtx& c = g_op[dev];
+  if (!c.err) {
+    CK(cudaMalloc(&c.err, sizeof(int)));
+    CK(cudaMemset(c.err, 0, sizeof(int)));
+  }
+  if (c.ws_bytes < ws_need) {
+    CK(cudaDeviceSynchronize());
+    if (c.ws) CK(cudaFree(c.ws));
+    c.ws = nullptr;
+    c.ws_bytes = 0;
+    CK(cudaMalloc(&c.ws, ws_need));
+    c.ws_bytes = ws_need;
+  }
+  if (c.n_tickets < tickets_need) {
+    CK(cudaDeviceSynchronize());
+    if (c.tickets) CK(cudaFree(c.tickets));
+    c.tickets = nullptr;
+    c.n_tickets = 0;
+    CK(cudaMalloc(&c.tickets, tickets_need * sizeof(unsigned int)));
+    CK(cudaMemset(c.tickets, 0, tickets_need * sizeof(unsigned int)));
+    c.n_tickets = tickets_need;
+  }
+  *out = &c;
+  return GPT_OK;
+}
+
+}  // namespace
+
+// ====================================================================== model
+
+struct LayerDev {
+  float *ln1_w = nullptr, *ln1_b = nullptr, *ln2_w = nullptr, *ln2_b = nullptr;
+  void *attn_w = nullptr, *proj_w = nullptr, *fc_w = nullptr, *mproj_w = nullptr;
+  float *attn_b = nullptr, *proj_b = nullptr, *fc_b = nullptr, *mproj_b = nullptr;
+};
+
+struct GraphKey {
+  int B = -1, T = -1, N = -1, top_k = 0;
+  float temperature = -1.0f;
+  unsigned long long seed = 0;
+  int* out = nullptr;
+  bool operator==(const GraphKey& o) const {
+    return B == o.B && T == o.T && N == o.N && top_k == o.top_k && temperature == o.temperature && seed == o.seed &&
+           out == o.out;
+  }
+};
+
+struct gpt_model {
+  gpt_config_t cfg{};
+  cudaStream_t stream = nullptr;
+  cudaStream_t cap_stream = nullptr;  // private stream used only to record the decode graph
+  int dev = 0, num_sms = 148;
+  bool bf16 = true;
+  size_t esz = 2;
+  int C = 0, nh = 0, hs = 64, L = 0, V = 0, block = 0, Bmax = 0;
+  std::vector<void*> allocs;
+  void* wte = nullptr;
+  void* wpe = nullptr;
+  float* ln_f_w = nullptr;
+  float* ln_f_b = nullptr;
+  std::vector<LayerDev> layers;
+  void* kv = nullptr;
+  float* x = nullptr;
+  void* xn = nullptr;
+  void* q = nullptr;
+  void* y = nullptr;
+  void* h = nullptr;
+  void* xf = nullptr;
+  float* logits = nullptr;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  unsigned int* tickets = nullptr;
+  size_t n_tickets = 0;
+  int* d_err = nullptr;
+  int* d_pos = nullptr;
+  int* d_step = nullptr;
+  int* d_tokens = nullptr;
+  int cache_len = 0, batch = 0;
+  bool hilo_decode = true;  // hi/lo bf16 operands for decode-step GEMMs (memory-bound, so free)
+  cudaGraphExec_t gexec = nullptr;
+  GraphKey gkey;
+  long long launches = 0;       // kernels enqueued so far (graph replays count every kernel node)
+  long long graph_kernels = 0;  // kernel nodes in the captured decode-step graph
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  bool timing_valid = false;
+  std::map<std::tuple<uintptr_t, long long, long long, int>, CUtensorMap> wmaps;
+
+  template <typename T>
+  T* alloc(size_t count, int* rc) {
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, count * sizeof(T));
+    if (e != cudaSuccess) {
+      *rc = cuda_fail(e, "cudaMalloc");
+      return nullptr;
+    }
+    allocs.push_back(p);
+    return static_cast<T*>(p);
+  }
+  void* alloc_bytes(size_t n, int* rc) { return alloc<uint8_t>(n, rc); }
+
+  void* kcache(int l) const { return static_cast<uint8_t*>(kv) + (static_cast<size_t>(l) * 2) * cache_layer_bytes(); }
+  void* vcache(int l) const {
+    return static_cast<uint8_t*>(kv) + (static_cast<size_t>(l) * 2 + 1) * cache_layer_bytes();
+  }
+  size_t cache_layer_bytes() const { return static_cast<size_t>(Bmax) * nh * block * hs * esz; }
+
+  int weight_map(const void* w, long long rows, long long cols, int box_rows, CUtensorMap* out) {
+    auto key = std::make_tuple(reinterpret_cast<uintptr_t>(w), rows, cols, box_rows);
+    auto it = wmaps.find(key);
+    if (it != wmaps.end()) {
+      *out = it->second;
+      return GPT_OK;
+    }
+    int rc = make_tmap(out, w, rows, cols, box_rows);
+    if (rc == GPT_OK) wmaps[key] = *out;
+    return rc;
+  }
+};
+
+namespace {
+
+void free_model(gpt_model* m) {
+  if (!m) return;
+  cudaStreamSynchronize(m->stream);
+  if (m->gexec) cudaGraphExecDestroy(m->gexec);
+  for (auto& e : m->ev)
+    if (e) cudaEventDestroy(e);
+  for (void* p : m->allocs) cudaFree(p);
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  delete m;
+}
+
+// y = A W^T with the given epilogue, bf16 operands.  A has M rows (2M with hilo).
+int gemm_bf16(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, bool hilo, int epi, Epi<bf16> e,
+              bool allow_split) {
+  GemmPlan p = plan_gemm(M, N, K, m->num_sms, hilo, m->ws_bytes);
+  if (!allow_split) p.splits = 1;
+  if (p.splits > 1 && static_cast<size_t>(cdiv(M, TC_BM)) * cdiv(N, p.bn) > m->n_tickets) p.splits = 1;
+  CUtensorMap ta, tb;
+  int rc = make_tmap(&ta, A, hilo ? 2LL * M : M, K, TC_BM);
+  if (rc) return rc;
+  rc = m->weight_map(W, N, K, p.bn, &tb);
+  if (rc) return rc;
+  e.M = M;
+  e.N = N;
+  e.splits = p.splits;
+  e.ws = m->ws;
+  e.tickets = m->tickets;
+  e.err = m->d_err;
+  CK(dispatch_tc(p.bn, hilo, epi, m->dev, ta, tb, M, N, K, p.splits, e, m->stream));
+  ++m->launches;
+  return GPT_OK;
+}
+
+template <int EPI>
+int gemm_f32(gpt_model* m, const float* A, const void* W, int M, int N, int K, Epi<float> e) {
+  e.M = M;
+  e.N = N;
+  e.err = m->d_err;
+  dim3 grid(cdiv(N, F32_BN), cdiv(M, F32_BM));
+  gemm_f32_kernel<EPI><<<grid, 256, 0, m->stream>>>(A, static_cast<const float*>(W), K, e);
+  CK(cudaGetLastError());
+  ++m->launches;
+  return GPT_OK;
+}
+
+int decode_attn_splits(const gpt_model* m, int B) {
+  const int pairs = B * m->nh;
+  int s = cdiv(2 * m->num_sms, pairs);
+  s = std::max(1, std::min(s, std::min(32, cdiv(m->block, 16))));
+  while (s > 1 && static_cast<size_t>(pairs) * s * (m->hs + 2) * sizeof(float) > m->ws_bytes) --s;
+  if (static_cast<size_t>(pairs) > m->n_tickets) s = 1;
+  return s;
+}
+
+// Enqueue the forward pass over B x T new tokens.  decode: T == 1 and the position comes
+// from m->d_pos; otherwise the tokens start at position 0.  Logits of each sequence's last
+// token go to logits (row stride V).
+template <typename TE>
+int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits) {
+  constexpr bool kBf16 = std::is_same<TE, bf16>::value;
+  const int C = m->C, nh = m->nh, V = m->V, rows = B * T;
+  const bool hilo = kBf16 && decode && m->hilo_decode;
+  const int* pos0 = decode ? m->d_pos : nullptr;
+  cudaStream_t st = m->stream;
+  TE* xn = static_cast<TE*>(m->xn);
+  TE* q = static_cast<TE*>(m->q);
+  TE* y = static_cast<TE*>(m->y);
+  TE* hbuf = static_cast<TE*>(m->h);
+  TE* xf = static_cast<TE*>(m->xf);
+  const int rows_per_cta = 8;  // 256 threads, warp per row
+
+  embed_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(tokens, rows, T, pos0, static_cast<const TE*>(m->wte),
+                                                               static_cast<const TE*>(m->wpe), V, m->block, C, m->x,
+                                                               m->d_err);
+  CK(cudaGetLastError());
+  ++m->launches;
+  for (int l = 0; l < m->L; ++l) {
+    const LayerDev& w = m->layers[l];
+    TE* kc = static_cast<TE*>(m->kcache(l));
+    TE* vc = static_cast<TE*>(m->vcache(l));
+    // ln_1
+    layernorm_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(m->x, rows, C, C, w.ln1_w, w.ln1_b, xn,
+                                                                    hilo ? xn + static_cast<size_t>(rows) * C : nullptr,
+                                                                    C);
+    CK(cudaGetLastError());
+    ++m->launches;
+    // c_attn + KV append
+    {
+      Epi<TE> e;
+      e.bias = w.attn_b;
+      e.q = q;
+      e.kc = kc;
+      e.vc = vc;
+      e.C = C;
+      e.nh = nh;
+      e.hs = m->hs;
+      e.T = T;
+      e.block = m->block;
+      e.pos0 = pos0;
+      int rc;
+      if constexpr (kBf16)
+        rc = gemm_bf16(m, xn, w.attn_w, rows, 3 * C, C, hilo, EPI_QKV, e, decode);
+      else
+        rc = gemm_f32<EPI_QKV>(m, xn, w.attn_w, rows, 3 * C, C, e);
+      if (rc) return rc;
+    }
+    // attention
+    if (decode) {
+      const int splits = decode_attn_splits(m, B);
+      TE* y_lo = hilo ? y + static_cast<size_t>(B) * C : nullptr;
+      if (m->hs == 64)
+        attn_decode_kernel<TE, 64><<<dim3(B * nh, splits), DEC_THREADS, 0, st>>>(
+            q, kc, vc, nh, m->block, m->d_pos, m->ws, m->tickets, y, y_lo, C, m->d_err);
+      else
+        attn_decode_kernel<TE, 32><<<dim3(B * nh, splits), DEC_THREADS, 0, st>>>(
+            q, kc, vc, nh, m->block, m->d_pos, m->ws, m->tickets, y, y_lo, C, m->d_err);
+    } else if constexpr (kBf16) {
+      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
+    } else {
+      if (m->hs == 64)
+        attn_prefill_f32<64><<<dim3(T, B * nh), 32, T * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
+      else
+        attn_prefill_f32<32><<<dim3(T, B * nh), 32, T * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
+    }
+    CK(cudaGetLastError());
+    ++m->launches;
+    // attn c_proj + residual
+    {
+      Epi<TE> e;
+      e.bias = w.proj_b;
+      e.x = m->x;
+      e.ldx = C;
+      int rc;
+      if constexpr (kBf16)
+        rc = gemm_bf16(m, y, w.proj_w, rows, C, C, hilo, EPI_RESID, e, decode);
+      else
+        rc = gemm_f32<EPI_RESID>(m, y, w.proj_w, rows, C, C, e);
+      if (rc) return rc;
+    }
+    // ln_2
+    layernorm_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(m->x, rows, C, C, w.ln2_w, w.ln2_b, xn,
+                                                                    hilo ? xn + static_cast<size_t>(rows) * C : nullptr,
+                                                                    C);
+    CK(cudaGetLastError());
+    ++m->launches;
+    // mlp c_fc + GELU
+    {
+      Epi<TE> e;
+      e.bias = w.fc_b;
+      e.out = hbuf;
+      e.out_lo = hilo ? hbuf + static_cast<size_t>(rows) * 4 * C : nullptr;
+      e.ldo = 4 * C;
+      int rc;
+      if constexpr (kBf16)
+        rc = gemm_bf16(m, xn, w.fc_w, rows, 4 * C, C, hilo, EPI_GELU, e, decode);
+      else
+        rc = gemm_f32<EPI_GELU>(m, xn, w.fc_w, rows, 4 * C, C, e);
+      if (rc) return rc;
+    }
+    // mlp c_proj + residual
+    {
+      Epi<TE> e;
+      e.bias = w.mproj_b;
+      e.x = m->x;
+      e.ldx = C;
+      int rc;
+      if constexpr (kBf16)
+        rc = gemm_bf16(m, hbuf, w.mproj_w, rows, C, 4 * C, hilo, EPI_RESID, e, decode);
+      else
+        rc = gemm_f32<EPI_RESID>(m, hbuf, w.mproj_w, rows, C, 4 * C, e);
+      if (rc) return rc;
+    }
+  }
+  // ln_f on the last position of each sequence, then the tied lm_head
+  layernorm_kernel<TE><<<cdiv(B, rows_per_cta), 256, 0, st>>>(
+      m->x + static_cast<size_t>(T - 1) * C, B, C, static_cast<long long>(T) * C, m->ln_f_w, m->ln_f_b, xf,
+      kBf16 ? xf + static_cast<size_t>(B) * C : nullptr, C);
+  CK(cudaGetLastError());
+  ++m->launches;
+  {
+    Epi<TE> e;
+    e.x = logits;
+    e.ldx = V;
+    int rc;
+    if constexpr (kBf16)
+      rc = gemm_bf16(m, xf, m->wte, B, V, C, true, EPI_F32, e, false);
+    else
+      rc = gemm_f32<EPI_F32>(m, xf, m->wte, B, V, C, e);
+    if (rc) return rc;
+  }
+  return GPT_OK;
+}
+
+int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits) {
+  return m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits)
+                 : enqueue_forward<float>(m, tokens, B, T, decode, logits);
+}
+
+int enqueue_sample(gpt_model* m, int B, float temperature, int top_k, unsigned long long seed, const int* step_dev,
+                   int step, int* out, int out_stride, int out_col0, cudaStream_t st) {
+  CK(set_sampler_smem(m->dev, m->V));
+  SampleArgs a;
+  a.logits = m->logits;
+  a.ld = m->V;
+  a.V = m->V;
+  a.temperature = temperature;
+  a.top_k = top_k;
+  a.seed = seed;
+  a.step_dev = step_dev;
+  a.step = step;
+  a.out = out;
+  a.out_stride = out_stride;
+  a.out_col0 = out_col0;
+  a.next_tokens = m->d_tokens;
+  a.thr_out = nullptr;
+  a.w_out = nullptr;
+  sample_kernel<<<B, SMP_THREADS, m->V * sizeof(float), st>>>(a);
+  CK(cudaGetLastError());
+  ++m->launches;
+  return GPT_OK;
+}
+
+template <typename TW>
+int copy_vec_f32(gpt_model* m, const void* src, size_t n, float** dst) {
+  int rc = GPT_OK;
+  *dst = m->alloc<float>(n, &rc);
+  if (!*dst) return rc;
+  widen_kernel<TW><<<std::min<long long>(1024, cdiv(n, 256)), 256, 0, m->stream>>>(static_cast<const TW*>(src), *dst,
+                                                                                    static_cast<long long>(n));
+  CK(cudaGetLastError());
+  return GPT_OK;
+}
+
+int copy_mat(gpt_model* m, const void* src, size_t n, void** dst) {
+  int rc = GPT_OK;
+  *dst = m->alloc_bytes(n * m->esz, &rc);
+  if (!*dst) return rc;
+  CK(cudaMemcpyAsync(*dst, src, n * m->esz, cudaMemcpyDeviceToDevice, m->stream));
+  return GPT_OK;
+}
+
+int copy_vec(gpt_model* m, const void* src, size_t n, float** dst) {
+  if (!src) {
+    *dst = nullptr;
+    return GPT_OK;
+  }
+  return m->bf16 ? copy_vec_f32<bf16>(m, src, n, dst) : copy_vec_f32<float>(m, src, n, dst);
+}
+
+int validate_config(const gpt_config_t* c) {
+  if (!c) return GPT_EINVAL;
+  if (c->n_layer < 0 || c->n_head < 1 || c->n_embd < 64 || c->n_embd % 64 != 0 || c->n_embd > 2048) return GPT_EINVAL;
+  const int hs = c->n_embd % c->n_head == 0 ? c->n_embd / c->n_head : 0;
+  if (hs != 64 && !(hs == 32 && c->dtype == GPT_DTYPE_F32)) return GPT_EINVAL;
+  if (c->dtype == GPT_DTYPE_F32 && c->block_size > 12288) return GPT_EINVAL;  // fp32 prefill keeps scores in smem
+  if (c->block_size < 1 || c->vocab_size < 1 || c->vocab_size > MAX_VOCAB) return GPT_EINVAL;
+  if ((c->bias != 0 && c->bias != 1) || (c->dtype != GPT_DTYPE_F32 && c->dtype != GPT_DTYPE_BF16)) return GPT_EINVAL;
+  if (c->max_batch < 1 || c->max_batch > 4096) return GPT_EINVAL;
+  return GPT_OK;
+}
+
+int create_impl(const gpt_config_t* cfg, const gpt_weights_t* w, void* stream, gpt_model* m) {
+  m->cfg = *cfg;
+  m->stream = static_cast<cudaStream_t>(stream);
+  CK(cudaGetDevice(&m->dev));
+  if (m->dev >= 64) return GPT_EUNSUPPORTED;
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, m->dev));
+  if (prop.major != 10 || prop.minor != 3) {
+    g_detail = std::string("device is ") + prop.name + " (sm_" + std::to_string(prop.major) +
+               std::to_string(prop.minor) + "); this library is built for sm_103a";
+    return GPT_EUNSUPPORTED;
+  }
+  if (!load_encode()) return GPT_EUNSUPPORTED;
+  m->num_sms = prop.multiProcessorCount;
+  CK(init_kernel_attrs(m->dev));
+  CK(set_sampler_smem(m->dev, cfg->vocab_size));
+  CK(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+  for (auto& e : m->ev) CK(cudaEventCreate(&e));
+  m->bf16 = cfg->dtype == GPT_DTYPE_BF16;
+  m->esz = m->bf16 ? 2 : 4;
+  m->C = cfg->n_embd;
+  m->nh = cfg->n_head;
+  m->hs = cfg->n_embd / cfg->n_head;
+  m->L = cfg->n_layer;
+  m->V = cfg->vocab_size;
+  m->block = cfg->block_size;
+  m->Bmax = cfg->max_batch;
+  const size_t C = m->C, V = m->V, blk = m->block, Bm = m->Bmax;
+  const bool has_bias = cfg->bias == 1;
+  int rc = GPT_OK;
+
+  // weights
+  if ((rc = copy_mat(m, w->wte, V * C, &m->wte))) return rc;
+  if ((rc = copy_mat(m, w->wpe, blk * C, &m->wpe))) return rc;
+  if ((rc = copy_vec(m, w->ln_f_w, C, &m->ln_f_w))) return rc;
+  if ((rc = copy_vec(m, has_bias ? w->ln_f_b : nullptr, C, &m->ln_f_b))) return rc;
+  m->layers.resize(m->L);
+  for (int l = 0; l < m->L; ++l) {
+    const gpt_layer_weights_t& s = w->layers[l];
+    LayerDev& d = m->layers[l];
+    if ((rc = copy_vec(m, s.ln_1_w, C, &d.ln1_w))) return rc;
+    if ((rc = copy_vec(m, has_bias ? s.ln_1_b : nullptr, C, &d.ln1_b))) return rc;
+    if ((rc = copy_mat(m, s.c_attn_w, 3 * C * C, &d.attn_w))) return rc;
+    if ((rc = copy_vec(m, has_bias ? s.c_attn_b : nullptr, 3 * C, &d.attn_b))) return rc;
+    if ((rc = copy_mat(m, s.attn_proj_w, C * C, &d.proj_w))) return rc;
+    if ((rc = copy_vec(m, has_bias ? s.attn_proj_b : nullptr, C, &d.proj_b))) return rc;
+    if ((rc = copy_vec(m, s.ln_2_w, C, &d.ln2_w))) return rc;
+    if ((rc = copy_vec(m, has_bias ? s.ln_2_b : nullptr, C, &d.ln2_b))) return rc;
+    if ((rc = copy_mat(m, s.c_fc_w, 4 * C * C, &d.fc_w))) return rc;
+    if ((rc = copy_vec(m, has_bias ? s.c_fc_b : nullptr, 4 * C, &d.fc_b))) return rc;
+    if ((rc = copy_mat(m, s.mlp_proj_w, 4 * C * C, &d.mproj_w))) return rc;
+    if ((rc = copy_vec(m, has_bias ? s.mlp_proj_b : nullptr, C, &d.mproj_b))) return rc;
+  }
+
+  // KV cache and activations
+  const size_t rows = std::max<size_t>(Bm * blk, 2 * Bm);
+  if (!(m->kv = m->alloc_bytes(static_cast<size_t>(m->L > 0 ? m->L : 1) * 2 * m->cache_layer_bytes(), &rc))) return rc;
+  CK(cudaMemsetAsync(m->kv, 0, static_cast<size_t>(m->L > 0 ? m->L : 1) * 2 * m->cache_layer_bytes(), m->stream));
+  if (!(m->x = m->alloc<float>(rows * C, &rc))) return rc;
+  if (!(m->xn = m->alloc_bytes(rows * C * m->esz, &rc))) return rc;
+  if (!(m->q = m->alloc_bytes(rows * C * m->esz, &rc))) return rc;
+  if (!(m->y = m->alloc_bytes(rows * C * m->esz, &rc))) return rc;
+  if (!(m->h = m->alloc_bytes(rows * 4 * C * m->esz, &rc))) return rc;
+  if (!(m->xf = m->alloc_bytes(2 * Bm * C * m->esz, &rc))) return rc;
+  if (!(m->logits = m->alloc<float>(Bm * V, &rc))) return rc;
+  // split-K / split-KV scratch: enough for a decode step at max_batch with up to 16 splits
+  m->ws_bytes = std::max<size_t>(16 * Bm * 4 * C * sizeof(float), Bm * m->nh * 32 * (m->hs + 2) * sizeof(float));
+  if (!(m->ws = m->alloc<float>(m->ws_bytes / sizeof(float), &rc))) return rc;
+  m->n_tickets = std::max<size_t>(4096, Bm * m->nh);
+  if (!(m->tickets = m->alloc<unsigned int>(m->n_tickets, &rc))) return rc;
+  CK(cudaMemsetAsync(m->tickets, 0, m->n_tickets * sizeof(unsigned int), m->stream));
+  if (!(m->d_err = m->alloc<int>(4, &rc))) return rc;
+  m->d_pos = m->d_err + 1;
+  m->d_step = m->d_err + 2;
+  CK(cudaMemsetAsync(m->d_err, 0, 4 * sizeof(int), m->stream));
+  if (!(m->d_tokens = m->alloc<int>(Bm, &rc))) return rc;
+  CK(cudaStreamSynchronize(m->stream));
+  return GPT_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* gpt_strerror(int code) {
+  switch (code) {
+    case GPT_OK: return "ok";
+    case GPT_EINVAL: return "invalid argument";
+    case GPT_ECONTEXT: return "context overflow: cache length + new tokens > block_size";
+    case GPT_ECUDA: return "CUDA error";
+    case GPT_ENOMEM: return "out of device memory";
+    case GPT_ETOKEN: return "token id out of range";
+    case GPT_ETIMEOUT: return "a kernel pipeline wait timed out";
+    case GPT_EPOSITION: return "position beyond block_size";
+    case GPT_EUNSUPPORTED: return "unsupported device or driver";
+    case GPT_ESTATE: return "call out of order";
+    default: return "unknown error";
+  }
+}
+
+const char* gpt_last_error_detail(void) { return g_detail.c_str(); }
+
+int gpt_create(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stream, gpt_model_t** out) {
+  if (!out) return GPT_EINVAL;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  if (!weights || !weights->wte || !weights->wpe || !weights->ln_f_w || (cfg->n_layer > 0 && !weights->layers))
+    return GPT_EINVAL;
+  if ((cfg->bias == 1) != (weights->ln_f_b != nullptr)) return GPT_EINVAL;
+  for (int l = 0; l < cfg->n_layer; ++l) {
+    const gpt_layer_weights_t& s = weights->layers[l];
+    if (!s.ln_1_w || !s.c_attn_w || !s.attn_proj_w || !s.ln_2_w || !s.c_fc_w || !s.mlp_proj_w) return GPT_EINVAL;
+    const bool all = s.ln_1_b && s.c_attn_b && s.attn_proj_b && s.ln_2_b && s.c_fc_b && s.mlp_proj_b;
+    const bool none = !s.ln_1_b && !s.c_attn_b && !s.attn_proj_b && !s.ln_2_b && !s.c_fc_b && !s.mlp_proj_b;
+    if (cfg->bias == 1 ? !all : !none) return GPT_EINVAL;
+  }
+  gpt_model* m = new gpt_model();
+  rc = create_impl(cfg, weights, stream, m);
+  if (rc) {
+    free_model(m);
+    return rc;
+  }
+  *out = m;
+  return GPT_OK;
+}
+
+void gpt_destroy(gpt_model_t* model) { free_model(model); }
+
+int32_t gpt_cache_length(const gpt_model_t* model) { return model ? model->cache_len : -1; }
+
+int64_t gpt_kernel_launches(const gpt_model_t* model) { return model ? model->launches : -1; }
+
+int gpt_prefill(gpt_model_t* m, const int32_t* tokens, int32_t B, int32_t T, float* logits) {
+  if (!m || !tokens || !logits || B < 1 || B > m->Bmax || T < 1) return GPT_EINVAL;
+  if (T > m->block) return GPT_ECONTEXT;
+  int rc = forward(m, tokens, B, T, false, logits);
+  if (rc) return rc;
+  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, T, nullptr, 0);
+  CK(cudaGetLastError());
+  ++m->launches;
+  m->cache_len = T;
+  m->batch = B;
+  return GPT_OK;
+}
+
+int gpt_decode_step(gpt_model_t* m, const int32_t* tokens, float* logits) {
+  if (!m || !tokens || !logits) return GPT_EINVAL;
+  if (m->batch < 1) return GPT_ESTATE;
+  if (m->cache_len + 1 > m->block) return GPT_ECONTEXT;
+  const int B = m->batch;
+  CK(cudaMemcpyAsync(m->d_tokens, tokens, B * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+  int rc = forward(m, m->d_tokens, B, 1, true, logits);
+  if (rc) return rc;
+  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, m->cache_len + 1, nullptr, 0);
+  CK(cudaGetLastError());
+  ++m->launches;
+  m->cache_len += 1;
+  return GPT_OK;
+}
+
+int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32_t max_new_tokens, float temperature,
+                 int32_t top_k, uint64_t seed, int32_t* out) {
+  if (!m || !idx || !out || B < 1 || B > m->Bmax || T < 1 || max_new_tokens < 1) return GPT_EINVAL;
+  if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return GPT_EINVAL;
+  if (static_cast<long long>(T) + max_new_tokens - 1 > m->block) return GPT_ECONTEXT;
+  const int N = max_new_tokens, W = T + N;
+  m->timing_valid = false;
+  CK(cudaEventRecord(m->ev[0], m->stream));
+  int rc = forward(m, idx, B, T, false, m->logits);
+  if (rc) return rc;
+  CK(cudaMemcpy2DAsync(out, W * sizeof(int), idx, T * sizeof(int), T * sizeof(int), B, cudaMemcpyDeviceToDevice,
+                       m->stream));
+  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, T, m->d_step, 1);
+  CK(cudaGetLastError());
+  ++m->launches;
+  if ((rc = enqueue_sample(m, B, temperature, top_k, seed, nullptr, 0, out, W, T, m->stream))) return rc;
+  CK(cudaEventRecord(m->ev[1], m->stream));
+  m->cache_len = T;
+  m->batch = B;
+  if (N > 1) {
+    GraphKey key;
+    key.B = B;
+    key.T = T;
+    key.N = N;
+    key.top_k = top_k;
+    key.temperature = temperature;
+    key.seed = seed;
+    key.out = out;
+    if (!m->gexec || !(m->gkey == key)) {
+      if (m->gexec) {
+        CK(cudaGraphExecDestroy(m->gexec));
+        m->gexec = nullptr;
+      }
+      cudaStream_t saved = m->stream;
+      const long long launches0 = m->launches;
+      m->stream = m->cap_stream;
+      CK(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+      rc = forward(m, m->d_tokens, B, 1, true, m->logits);
+      if (!rc) rc = enqueue_sample(m, B, temperature, top_k, seed, m->d_step, 0, out, W, T, m->cap_stream);
+      if (!rc) {
+        advance_kernel<<<1, 1, 0, m->cap_stream>>>(m->d_pos, m->d_step);
+        if (cudaGetLastError() != cudaSuccess) rc = GPT_ECUDA;
+        ++m->launches;
+      }
+      m->graph_kernels = m->launches - launches0;
+      m->launches = launches0;
+      cudaGraph_t graph = nullptr;
+      cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &graph);
+      m->stream = saved;
+      if (rc) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+      }
+      if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamEndCapture");
+      ce = cudaGraphInstantiate(&m->gexec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (ce != cudaSuccess) return cuda_fail(ce, "cudaGraphInstantiate");
+      m->gkey = key;
+    }
+    for (int j = 1; j < N; ++j) {
+      CK(cudaGraphLaunch(m->gexec, m->stream));
+      m->launches += m->graph_kernels;
+    }
+    m->cache_len = T + N - 1;
+  }
+  CK(cudaEventRecord(m->ev[2], m->stream));
+  m->timing_valid = true;
+  return GPT_OK;
+}
+
+int gpt_last_timing(gpt_model_t* m, float* prefill_ms, float* decode_ms) {
+  if (!m) return GPT_EINVAL;
+  if (!m->timing_valid) return GPT_ESTATE;
+  CK(cudaEventSynchronize(m->ev[2]));
+  float a = 0.0f, b = 0.0f;
+  CK(cudaEventElapsedTime(&a, m->ev[0], m->ev[1]));
+  CK(cudaEventElapsedTime(&b, m->ev[1], m->ev[2]));
+  if (prefill_ms) *prefill_ms = a;
+  if (decode_ms) *decode_ms = b;
+  return GPT_OK;
+}
+
+int gpt_sync_status(gpt_model_t* m) {
+  if (!m) return GPT_EINVAL;
+  CK(cudaStreamSynchronize(m->stream));
+  int w = 0;
+  CK(cudaMemcpy(&w, m->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  CK(cudaMemcpy(m->d_err, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  return map_error_word(w);
+}
+
+// ------------------------------------------------------------------ stand-alone operations
+
+int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
+                    int32_t hilo, int32_t block_n, int32_t splits, void* stream) {
+  if (!A || !W || !out || M < 1 || N < 1 || K < 64 || K % 64 != 0 || splits < 1) return GPT_EINVAL;
+  if (block_n != 0 && block_n != 64 && block_n != 128 && block_n != 256) return GPT_EINVAL;
+  if (hilo && block_n == 256) return GPT_EINVAL;
+  if (splits > 1 && N % 16 != 0) return GPT_EINVAL;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  int num_sms = 148;
+  CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  GemmPlan p = plan_gemm(M, N, K, num_sms, hilo != 0, ~size_t(0));
+  if (block_n) p.bn = block_n;
+  p.splits = std::min(splits, K / TC_BK);
+  p.splits = cdiv(K / TC_BK, cdiv(K / TC_BK, p.splits));
+  OpCtx* c = nullptr;
+  const size_t tiles = static_cast<size_t>(cdiv(M, TC_BM)) * cdiv(N, p.bn);
+  int rc = op_ctx(&c, p.splits > 1 ? static_cast<size_t>(p.splits) * M * N * sizeof(float) : 256, tiles);
+  if (rc) return rc;
+  CUtensorMap ta, tb;
+  if ((rc = make_tmap(&ta, A, hilo ? 2LL * M : M, K, TC_BM))) return rc;
+  if ((rc = make_tmap(&tb, W, N, K, p.bn))) return rc;
+  Epi<bf16> e;
+  e.M = M;
+  e.N = N;
+  e.bias = bias;
+  e.x = out;
+  e.ldx = N;
+  e.splits = p.splits;
+  e.ws = c->ws;
+  e.tickets = c->tickets;
+  e.err = c->err;
+  CK(dispatch_tc(p.bn, hilo != 0, EPI_F32, dev, ta, tb, M, N, K, p.splits, e, static_cast<cudaStream_t>(stream)));
+  return GPT_OK;
+}
+
+int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const float* beta, int32_t rows, int32_t C,
+                  int32_t dtype, void* y, void* y_lo, void* stream) {
+  if (!x || !gamma || !y || rows < 1 || C < 64 || C % 64 != 0 || C > 64 * LN_MAX_PAIRS || x_stride < C) return GPT_EINVAL;
+  if (dtype != GPT_DTYPE_BF16 && dtype != GPT_DTYPE_F32) return GPT_EINVAL;
+  if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == GPT_DTYPE_BF16)
+    layernorm_kernel<bf16><<<cdiv(rows, 8), 256, 0, st>>>(x, rows, C, x_stride, gamma, beta, static_cast<bf16*>(y),
+                                                          static_cast<bf16*>(y_lo), C);
+  else
+    layernorm_kernel<float><<<cdiv(rows, 8), 256, 0, st>>>(x, rows, C, x_stride, gamma, beta, static_cast<float*>(y),
+                                                           nullptr, C);
+  CK(cudaGetLastError());
+  return GPT_OK;
+}
+
+int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
+                          int32_t n_head, int32_t head_size, int32_t T, int32_t block, int32_t pos0, void* y,
+                          void* stream) {
+  if (!q || !k_cache || !v_cache || !y || B < 1 || n_head < 1 || T < 1 || pos0 < 0 || pos0 + T > block)
+    return GPT_EINVAL;
+  if (head_size != 64 && !(head_size == 32 && dtype == GPT_DTYPE_F32)) return GPT_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int C = head_size * n_head;
+  if (dtype == GPT_DTYPE_BF16) {
+    attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * n_head), PF_THREADS, 0, st>>>(
+        static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache), static_cast<const bf16*>(v_cache), n_head, T,
+        block, pos0, static_cast<bf16*>(y), C);
+  } else if (dtype == GPT_DTYPE_F32) {
+    if ((pos0 + T) * sizeof(float) > 48 * 1024) return GPT_EINVAL;
+    auto kern = head_size == 64 ? attn_prefill_f32<64> : attn_prefill_f32<32>;
+    kern<<<dim3(T, B * n_head), 32, (pos0 + T) * sizeof(float), st>>>(
+        static_cast<const float*>(q), static_cast<const float*>(k_cache), static_cast<const float*>(v_cache), n_head,
+        T, block, pos0, static_cast<float*>(y), C);
+  } else {
+    return GPT_EINVAL;
+  }
+  CK(cudaGetLastError());
+  return GPT_OK;
+}
+
+int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
+                         int32_t n_head, int32_t head_size, int32_t block, const int32_t* pos0_dev, int32_t splits,
+                         void* y, void* y_lo, void* stream) {
+  if (!q || !k_cache || !v_cache || !y || !pos0_dev || B < 1 || n_head < 1 || block < 1 || splits < 1 ||
+      splits > 1024)
+    return GPT_EINVAL;
+  if (head_size != 64 && head_size != 32) return GPT_EINVAL;
+  if (dtype != GPT_DTYPE_BF16 && dtype != GPT_DTYPE_F32) return GPT_EINVAL;
+  if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;
+  const size_t pairs = static_cast<size_t>(B) * n_head;
+  OpCtx* c = nullptr;
+  int rc = op_ctx(&c, pairs * splits * (head_size + 2) * sizeof(float), pairs);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int C = head_size * n_head;
+  const dim3 grid(B * n_head, splits);
+  if (dtype == GPT_DTYPE_BF16) {
+    auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
+    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
+                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, c->ws, c->tickets,
+                                       static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, c->err);
+  } else {
+    auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
+    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
+                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, c->ws, c->tickets,
+                                       static_cast<float*>(y), nullptr, C, c->err);
+  }
+  CK(cudaGetLastError());
+  return GPT_OK;
+}
+
+int gpt_sample(const float* logits, int32_t B, int32_t V, float temperature, int32_t top_k, uint64_t seed,
+               int32_t step, int32_t* tokens, float* thresholds, uint64_t* weights, void* stream) {
+  if (!logits || !tokens || B < 1 || V < 1 || V > MAX_VOCAB || !(temperature >= 0.0f) || !std::isfinite(temperature))
+    return GPT_EINVAL;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  CK(set_sampler_smem(dev, V));
+  SampleArgs a;
+  a.logits = logits;
+  a.ld = V;
+  a.V = V;
+  a.temperature = temperature;
+  a.top_k = top_k;
+  a.seed = seed;
+  a.step_dev = nullptr;
+  a.step = step;
+  a.out = nullptr;
+  a.out_stride = 0;
+  a.out_col0 = 0;
+  a.next_tokens = tokens;
+  a.thr_out = thresholds;
+  a.w_out = reinterpret_cast<unsigned long long*>(weights);
+  sample_kernel<<<B, SMP_THREADS, V * sizeof(float), static_cast<cudaStream_t>(stream)>>>(a);
+  CK(cudaGetLastError());
+  return GPT_OK;
+}
+
+int gpt_op_status(void) {
+  OpCtx* c = nullptr;
+  int rc = op_ctx(&c, 0, 0);
+  if (rc) return rc;
+  CK(cudaDeviceSynchronize());
+  int w = 0;
+  CK(cudaMemcpy(&w, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+  const int zero = 0;
+  CK(cudaMemcpy(c->err, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  return map_error_word(w);
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// Token + position embedding, and LayerNorm (warp per row, one read of the row).
+//
+// Embedding ("第 4 章 模型构建", aiknowledge.cn, §4.5): x = wte[id] + wpe[pos], learned
+// absolute positions; a new token appended to a cache of length c sits at position c.
+// LayerNorm ("原生 nanoGPT 模型服务首选", §1): F.layer_norm with eps 1e-5, biased
+// variance, gamma, and an optional beta (bias=False passes no beta).
+#pragma once
+
+#include "common.cuh"
+
+namespace kvgpt {
+
+constexpr int LN_MAX_PAIRS = 32;  // up to C = 2048 (C/64 float pairs per lane)
+
+// rows = B*T; row r = b*T + t embeds tokens[r] at position pos0 + t into x[r, :] (fp32).
+// A token outside [0, V) or a position >= block sets the error word and writes zeros.
+template <typename TW>
+__global__ void embed_kernel(const int* __restrict__ tokens, int rows, int T, const int* pos0,
+                             const TW* __restrict__ wte, const TW* __restrict__ wpe, int V, int block, int C,
+                             float* __restrict__ x, int* err) {
+  const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const int t = r % T;
+  const int tok = tokens[r];
+  const int pos = (pos0 ? *pos0 : 0) + t;
+  float* xr = x + static_cast<size_t>(r) * C;
+  const bool bad_tok = tok < 0 || tok >= V;
+  const bool bad_pos = pos >= block;
+  if (bad_tok || bad_pos) {
+    if (lane == 0) atomicOr(err, bad_tok ? ERR_TOKEN : ERR_POSITION);
+    for (int c = lane; c < C; c += 32) xr[c] = 0.0f;
+    return;
+  }
+  const TW* we = wte + static_cast<size_t>(tok) * C;
+  const TW* pe = wpe + static_cast<size_t>(pos) * C;
+  for (int c = lane * 2; c < C; c += 64) {
+    float2 o;
+    o.x = to_f32(we[c]) + to_f32(pe[c]);
+    o.y = to_f32(we[c + 1]) + to_f32(pe[c + 1]);
+    *reinterpret_cast<float2*>(xr + c) = o;
+  }
+}
+
+// y[r, :] = LN(x[r * in_stride + :]) for r < rows; warp per row.  TO is bf16 or f32.
+// With y_lo, also writes the rounding remainder y - bf16(y) (the lo half of a hi/lo pair).
+template <typename TO>
+__global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, long long in_stride,
+                                 const float* __restrict__ gamma, const float* __restrict__ beta,
+                                 TO* __restrict__ y, TO* __restrict__ y_lo, int ldy) {
+  const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const float* xr = x + static_cast<size_t>(r) * in_stride;
+  const int np = C / 64;
+  float2 v[LN_MAX_PAIRS];
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+    if (i < np) {
+      v[i] = *reinterpret_cast<const float2*>(xr + i * 64 + lane * 2);
+      s += v[i].x + v[i].y;
+    }
+  }
+  const float mean = warp_sum(s) / static_cast<float>(C);
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+    if (i < np) {
+      const float a = v[i].x - mean, b = v[i].y - mean;
+      q += a * a + b * b;
+    }
+  }
+  const float var = warp_sum(q) / static_cast<float>(C);
+  const float rstd = 1.0f / sqrtf(var + 1e-5f);
+  TO* yr = y + static_cast<size_t>(r) * ldy;
+#pragma unroll
+  for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+    if (i < np) {
+      const int c = i * 64 + lane * 2;
+      float a = (v[i].x - mean) * rstd * gamma[c];
+      float b = (v[i].y - mean) * rstd * gamma[c + 1];
+      if (beta) {
+        a += beta[c];
+        b += beta[c + 1];
+      }
+      const TO ha = from_f32<TO>(a), hb = from_f32<TO>(b);
+      yr[c] = ha;
+      yr[c + 1] = hb;
+      if (y_lo) {
+        TO* lr = y_lo + static_cast<size_t>(r) * ldy;
+        lr[c] = from_f32<TO>(a - to_f32(ha));
+        lr[c + 1] = from_f32<TO>(b - to_f32(hb));
+      }
+    }
+  }
+}
+
+// Widen a weight vector to fp32 (LayerNorm parameters and biases are kept in fp32).
+template <typename TW>
+__global__ void widen_kernel(const TW* __restrict__ src, float* __restrict__ dst, long long n) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    dst[i] = to_f32(src[i]);
+}
+
+}  // namespace kvgpt

@@ -1,0 +1,182 @@
+"""Whole-model parity through the C ABI: teacher-forced logits against the oracle (GPU).
+
+Tolerances: fp32 model 1e-3 max abs on every step's logits; bf16 models 5e-2 max abs
+and at least 99% agreement of the greedy argmax over all checked (row, step) pairs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kv_cached_generation_gpt_b300 import gpt as G
+from kv_cached_generation_gpt_b300 import synthetic as syn
+from oracle import gpt as og
+from oracle import sampler as osm
+
+from gpu_common import argmax_agreement, gpu_teacher_forced, make_gpu_model, oracle_model
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 5e-2
+F32_TOL = 1e-3
+
+
+def _weights(wl: syn.Workload):
+    return syn.make_weights(wl.model, bias_std=wl.bias_std)
+
+
+def test_tiny_f32_greedy_teacher_forced():
+    """tiny_b1_p16_d32: fp32 weights, 32 greedy decode steps, the oracle's greedy tokens fed to both."""
+    wl = syn.WORKLOADS["tiny_b1_p16_d32"]
+    sd = _weights(wl)
+    cfg, w = oracle_model(wl.model, sd)
+    prompt = syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)
+    fed, ref = og.teacher_forced(cfg, w, prompt, n_steps=wl.decode_steps)
+    model = make_gpu_model(wl.model, sd, wl.batch)
+    got = gpu_teacher_forced(model, prompt, fed)
+    assert got.shape == ref.shape
+    assert np.max(np.abs(got - ref)) < F32_TOL
+    assert argmax_agreement(got, ref) == 1.0
+    assert model.cache_length == wl.prompt + wl.decode_steps
+
+
+@pytest.mark.parametrize("shape,B,P,N,bias_std", [
+    (syn.ModelShape(2, 2, 128, 96, 300, True, "bf16"), 3, 9, 20, 0.05),
+    (syn.ModelShape(3, 3, 192, 80, 1000, False, "bf16"), 2, 65, 15, None),  # C % 128 != 0, ragged prompt tile
+    (syn.ModelShape(1, 4, 256, 64, 129, True, "f32"), 2, 30, 34, None),     # fills block_size exactly
+])
+def test_small_models_teacher_forced(shape, B, P, N, bias_std):
+    sd = syn.make_weights(shape, seed=21, bias_std=bias_std, random_gamma=True)
+    cfg, w = oracle_model(shape, sd)
+    prompt = syn.make_tokens(B, P, shape.vocab_size, seed=3)
+    forced = syn.make_tokens(B, N, shape.vocab_size, seed=4)
+    _, ref = og.teacher_forced(cfg, w, prompt, forced)
+    got = gpu_teacher_forced(make_gpu_model(shape, sd, B + 1), prompt, forced)
+    tol = F32_TOL if shape.dtype == "f32" else BF16_TOL
+    assert np.max(np.abs(got - ref)) < tol
+    assert argmax_agreement(got, ref) >= 0.99
+
+
+def test_char_b1_p1_d255_sampled_tokens_teacher_forced():
+    """char_b1_p1_d255: the oracle's own temperature-0.8 / top-200 draws are fed to both sides."""
+    wl = syn.WORKLOADS["char_b1_p1_d255"]
+    sd = _weights(wl)
+    cfg, w = oracle_model(wl.model, sd)
+    prompt = syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)
+    seq = og.generate(cfg, w, prompt, wl.decode_steps + 1, wl.temperature, wl.top_k, seed=5)
+    forced = seq[:, wl.prompt:wl.prompt + wl.decode_steps]
+    _, ref = og.teacher_forced(cfg, w, prompt, forced)
+    got = gpu_teacher_forced(make_gpu_model(wl.model, sd, wl.batch), prompt, forced)
+    assert np.max(np.abs(got - ref)) < BF16_TOL
+    assert argmax_agreement(got, ref) >= 0.99
+
+
+def test_gpt2_124m_b1_greedy_teacher_forced():
+    """gpt2_124m_b1_p128_d896: 896 greedy steps, the oracle's greedy tokens fed to both (fills 1024)."""
+    wl = syn.WORKLOADS["gpt2_124m_b1_p128_d896"]
+    sd = _weights(wl)
+    cfg, w = oracle_model(wl.model, sd)
+    prompt = syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)
+    fed, ref = og.teacher_forced(cfg, w, prompt, n_steps=wl.decode_steps)
+    got = gpu_teacher_forced(make_gpu_model(wl.model, sd, wl.batch), prompt, fed)
+    err = np.max(np.abs(got - ref))
+    agree = argmax_agreement(got, ref)
+    print(f"gpt2_124m B=1: max|err| {err:.3e}, argmax agreement {agree:.4f}")
+    assert err < BF16_TOL
+    assert agree >= 0.99
+
+
+@pytest.mark.parametrize("name,rows", [("gpt2_124m_b64_p512_d512", [0, 21, 63]), ("gpt2_350m_b8_p768_d256", [0, 7])])
+def test_full_size_sampled_rows(name, rows):
+    """Full batch and cache at the benchmark's sizes; sampled rows are checked at every
+    position against the oracle's no-cache forward over the whole fed sequence."""
+    wl = syn.WORKLOADS[name]
+    sd = _weights(wl)
+    prompt = syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)
+    forced = syn.make_tokens(wl.batch, wl.decode_steps, wl.token_hi, seed=77)
+    model = make_gpu_model(wl.model, sd, wl.batch)
+    got = gpu_teacher_forced(model, prompt, forced, rows=rows)  # (N+1, rows, V)
+    assert model.cache_length == wl.prompt + wl.decode_steps == wl.model.block_size
+    del model
+    cfg, w = oracle_model(wl.model, sd)
+    errs, agree = [], []
+    for i, r in enumerate(rows):
+        seq = np.concatenate([prompt[r:r + 1], forced[r:r + 1]], axis=1)
+        full = og.forward_full(cfg, w, seq)[0, wl.prompt - 1:]  # positions P-1 .. P+N-1
+        errs.append(np.max(np.abs(got[:, i] - full)))
+        agree.append(np.argmax(got[:, i], axis=-1) == np.argmax(full, axis=-1))
+    agree = float(np.mean(np.concatenate(agree)))
+    print(f"{name}: max|err| {max(errs):.3e}, argmax agreement {agree:.4f}")
+    assert max(errs) < BF16_TOL
+    assert agree >= 0.99
+
+
+def test_generate_matches_step_by_step_and_oracle_sampler():
+    """gpt_generate (prefill + graph-replayed decode + draws) equals the same draws made with
+    gpt_prefill / gpt_decode_step / gpt_sample, and the oracle's sampler on the GPU logits."""
+    shape = syn.ModelShape(2, 2, 128, 64, 500, True, "bf16")
+    sd = syn.make_weights(shape, seed=8, bias_std=0.02)
+    B, T, N, temp, k, seed = 3, 5, 20, 0.9, 40, 4242
+    prompt = torch.from_numpy(syn.make_tokens(B, T, 500, seed=6)).cuda()
+    model = make_gpu_model(shape, sd, B)
+    out = model.generate(prompt, N, temperature=temp, top_k=k, seed=seed)
+    assert model.sync_status() == G.GPT_OK
+    assert torch.equal(out[:, :T], prompt)
+    assert model.cache_length == T + N - 1
+    pre, dec = G.gpt_last_timing(model.handle)
+    assert pre > 0 and dec > 0
+    # replay the same computation step by step
+    logits = model.prefill(prompt)
+    toks = []
+    for j in range(N):
+        tok = torch.empty(B, dtype=torch.int32, device="cuda")
+        G.gpt_sample(logits, temp, k, seed, j, tok)
+        toks.append(tok)
+        ref = np.array([osm.sample_row(logits[b].cpu().numpy(), temp, k, seed, b, j) for b in range(B)])
+        assert np.array_equal(tok.cpu().numpy(), ref)
+        if j + 1 < N:
+            logits = model.decode_step(tok)
+    assert torch.equal(out[:, T:], torch.stack(toks, dim=1))
+    # a second generate reuses the captured graph and gives the same tokens
+    out2 = model.generate(prompt, N, temperature=temp, top_k=k, seed=seed)
+    assert torch.equal(out, out2)
+
+
+def test_generate_greedy_equals_oracle_greedy_on_fp32_model():
+    wl = syn.WORKLOADS["tiny_b1_p16_d32"]
+    sd = _weights(wl)
+    cfg, w = oracle_model(wl.model, sd)
+    prompt = syn.make_tokens(2, 16, 65, seed=2)
+    ref = og.generate(cfg, w, prompt, 40, 0.0, None, 0)
+    model = make_gpu_model(wl.model, sd, 2)
+    out = model.generate(torch.from_numpy(prompt).cuda(), 40, temperature=0.0)
+    assert model.sync_status() == G.GPT_OK
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_error_paths():
+    shape = syn.ModelShape(1, 2, 128, 16, 100, False, "bf16")
+    sd = syn.make_weights(shape, seed=1)
+    model = make_gpu_model(shape, sd, 2)
+    h = model.handle
+    logits = torch.empty(3, 100, device="cuda")
+    tok = torch.zeros(3, 16, dtype=torch.int32, device="cuda")
+    assert G.lib().gpt_decode_step(h, tok.data_ptr(), logits.data_ptr()) == G.GPT_ESTATE
+    assert G.lib().gpt_prefill(h, tok.data_ptr(), 3, 4, logits.data_ptr()) == G.GPT_EINVAL  # B > max_batch
+    assert G.lib().gpt_prefill(h, tok.data_ptr(), 1, 17, logits.data_ptr()) == G.GPT_ECONTEXT
+    assert G.lib().gpt_generate(h, tok.data_ptr(), 1, 10, 8, 1.0, 0, 0, logits.data_ptr()) == G.GPT_ECONTEXT
+    assert G.lib().gpt_generate(h, tok.data_ptr(), 1, 4, 2, float("nan"), 0, 0, logits.data_ptr()) == G.GPT_EINVAL
+    # a token id out of range is flagged by the device error word; its embedding row is zeroed
+    bad = torch.tensor([[1, 2, 100]], dtype=torch.int32, device="cuda")
+    model.prefill(bad)
+    assert model.sync_status() == G.GPT_ETOKEN
+    assert model.sync_status() == G.GPT_OK  # cleared
+    good = torch.tensor([[1, 2, 3]], dtype=torch.int32, device="cuda")
+    model.prefill(good)
+    for _ in range(13):
+        model.decode_step(torch.tensor([5], dtype=torch.int32, device="cuda"))
+    assert model.cache_length == 16
+    with pytest.raises(G.GptError) as ei:
+        model.decode_step(torch.tensor([5], dtype=torch.int32, device="cuda"))
+    assert ei.value.code == G.GPT_ECONTEXT
+    assert model.sync_status() == G.GPT_OK
+    model.close()

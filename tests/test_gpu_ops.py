@@ -1,0 +1,248 @@
+"""Per-kernel parity of the stand-alone C-ABI operations against the oracle (GPU)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cached_generation_gpt_b300 import gpt as G
+from kv_cached_generation_gpt_b300 import synthetic as syn
+from oracle import gpt as og
+from oracle import sampler as osm
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _ok():
+    assert G.gpt_op_status() == G.GPT_OK
+
+
+# ------------------------------------------------------------------ tcgen05 GEMM
+
+
+@pytest.mark.parametrize("M,N,K,block_n,splits,hilo", [
+    (1, 64, 64, 64, 1, False),
+    (5, 192, 128, 64, 1, False),
+    (128, 128, 256, 128, 1, False),
+    (130, 256, 768, 256, 1, False),       # two M tiles, ragged
+    (300, 2304, 768, 0, 1, False),        # QKV shape, library-chosen tile
+    (64, 3072, 768, 64, 4, False),        # decode fc with split-K
+    (64, 768, 3072, 64, 12, True),        # decode proj, split-K, hi/lo operand
+    (3, 50304, 768, 128, 1, True),        # lm_head shape, hi/lo
+    (2, 50257, 1024, 64, 1, True),        # ragged vocabulary (N % 16 != 0)
+    (1000, 1024, 4096, 256, 1, False),    # 350M mlp proj, several tiles each way
+])
+def test_linear_bf16_matches_definition(M, N, K, block_n, splits, hilo):
+    r = _rng(M * 7 + N + K)
+    a = r.standard_normal((M, K)).astype(np.float32)
+    w = (r.standard_normal((N, K)) * 0.05).astype(np.float32)
+    b = (r.standard_normal(N) * 0.1).astype(np.float32)
+    A_hi = _bf16(a)
+    if hilo:
+        A_lo = _bf16(a - A_hi.float().numpy())
+        A = torch.cat([A_hi, A_lo]).cuda()
+        a_eff = _f64(A_hi) + _f64(A_lo)
+    else:
+        A = A_hi.cuda()
+        a_eff = _f64(A_hi)
+    W = _bf16(w).cuda()
+    bias = torch.from_numpy(b).cuda()
+    out = torch.full((M, N), float("nan"), device="cuda")
+    G.gpt_linear_bf16(A, W, bias, out, M, hilo=hilo, block_n=block_n, splits=splits)
+    _ok()
+    ref = og.linear(a_eff, _f64(W), b.astype(np.float64))
+    got = out.cpu().numpy().astype(np.float64)
+    # fp32 accumulation of K exact products
+    tol = 2e-6 * math.sqrt(K) * np.max(np.abs(a_eff)) * np.max(np.abs(_f64(W))) * 4 + 1e-6
+    assert np.max(np.abs(got - ref)) < tol
+    if hilo:  # the hi/lo pair reproduces the fp32 operand far better than bf16 alone
+        assert np.max(np.abs(got - og.linear(a.astype(np.float64), _f64(W), b))) < 50 * tol
+
+
+def test_linear_split_k_is_deterministic():
+    r = _rng(3)
+    A = _bf16(r.standard_normal((64, 3072))).cuda()
+    W = _bf16(r.standard_normal((768, 3072)) * 0.02).cuda()
+    outs = []
+    for _ in range(3):
+        o = torch.empty(64, 768, device="cuda")
+        G.gpt_linear_bf16(A, W, None, o, 64, splits=12, block_n=64)
+        outs.append(o.cpu())
+    _ok()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+# ------------------------------------------------------------------ LayerNorm
+
+
+@pytest.mark.parametrize("C,rows,with_beta", [(128, 1, False), (384, 7, True), (768, 300, False), (1024, 33, True),
+                                              (2048, 5, True)])
+def test_layernorm_matches_oracle(C, rows, with_beta):
+    r = _rng(C + rows)
+    x = (r.standard_normal((rows, C)) * 3 + 0.5).astype(np.float32)
+    g = (1 + 0.1 * r.standard_normal(C)).astype(np.float32)
+    be = (0.1 * r.standard_normal(C)).astype(np.float32) if with_beta else None
+    ref = og.layer_norm(x.astype(np.float64), g.astype(np.float64), None if be is None else be.astype(np.float64))
+    xd, gd = torch.from_numpy(x).cuda(), torch.from_numpy(g).cuda()
+    bd = None if be is None else torch.from_numpy(be).cuda()
+    y32 = torch.empty(rows, C, device="cuda")
+    G.gpt_layernorm(xd, gd, bd, y32)
+    yh = torch.empty(rows, C, device="cuda", dtype=torch.bfloat16)
+    yl = torch.empty_like(yh)
+    G.gpt_layernorm(xd, gd, bd, yh, yl)
+    _ok()
+    assert np.max(np.abs(y32.cpu().numpy() - ref)) < 2e-5
+    assert np.max(np.abs(_f64(yh) - ref) / (np.abs(ref) + 1e-3)) < 2 ** -8 + 1e-3
+    assert np.max(np.abs(_f64(yh) + _f64(yl) - ref)) < 4e-5
+
+
+def test_layernorm_strided_rows_pick_last_positions():
+    B, T, C = 3, 5, 256
+    x = _rng(1).standard_normal((B, T, C)).astype(np.float32)
+    g = np.ones(C, np.float32)
+    ref = og.layer_norm(x[:, -1].astype(np.float64), g.astype(np.float64), None)
+    xd = torch.from_numpy(x).cuda()
+    y = torch.empty(B, C, device="cuda")
+    last = xd.view(-1)[(T - 1) * C:]  # row b starts at (b*T + T-1) * C
+    G.gpt_layernorm(last, torch.from_numpy(g).cuda(), None, y, x_stride=T * C, rows=B)
+    _ok()
+    assert np.max(np.abs(y.cpu().numpy() - ref)) < 2e-5
+
+
+# ------------------------------------------------------------------ attention
+
+
+def _cache(r, B, nh, block, n, dt, hs=64):
+    k = np.zeros((B, nh, block, hs), np.float32)
+    v = np.zeros((B, nh, block, hs), np.float32)
+    k[:, :, :n] = r.standard_normal((B, nh, n, hs))
+    v[:, :, :n] = r.standard_normal((B, nh, n, hs))
+    k[:, :, n:] = np.nan  # rows beyond the live length must never be read
+    v[:, :, n:] = np.nan
+    return torch.from_numpy(k).to(dt).cuda(), torch.from_numpy(v).to(dt).cuda()
+
+
+@pytest.mark.parametrize("dt,hs", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float32, 32)])
+@pytest.mark.parametrize("B,nh,T,pos0,block", [(1, 1, 1, 0, 8), (2, 3, 17, 0, 32), (1, 2, 64, 0, 64),
+                                               (2, 2, 100, 0, 128), (1, 12, 129, 0, 256), (2, 2, 37, 50, 128)])
+def test_attention_prefill_matches_oracle(dt, hs, B, nh, T, pos0, block):
+    r = _rng(B * 100 + T + pos0)
+    q = torch.from_numpy(r.standard_normal((B, nh, T, hs)).astype(np.float32)).to(dt).cuda()
+    kc, vc = _cache(r, B, nh, block, pos0 + T, dt, hs)
+    y = torch.full((B * T, nh * hs), float("nan"), device="cuda", dtype=dt)
+    G.gpt_attention_prefill(q, kc, vc, pos0, y)
+    _ok()
+    n = pos0 + T
+    ref = og.attention(_f64(q), _f64(kc[:, :, :n]), _f64(vc[:, :, :n]), q_pos0=pos0)  # (B, nh, T, hs)
+    ref = ref.transpose(0, 2, 1, 3).reshape(B * T, nh * hs)
+    tol = 1.5e-2 if dt == torch.bfloat16 else 2e-5
+    assert np.max(np.abs(_f64(y) - ref)) < tol
+
+
+@pytest.mark.parametrize("dt,hs", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float32, 32),
+                                   (torch.bfloat16, 32)])
+@pytest.mark.parametrize("B,nh,t,splits,block", [(1, 1, 1, 1, 8), (1, 12, 129, 8, 1024), (3, 2, 1024, 1, 1024),
+                                                 (2, 4, 77, 3, 96), (64, 12, 600, 1, 1024), (1, 12, 1000, 32, 1024)])
+def test_attention_decode_matches_oracle(dt, hs, B, nh, t, splits, block):
+    r = _rng(B + nh * 10 + t)
+    q = torch.from_numpy(r.standard_normal((B, nh, 1, hs)).astype(np.float32)).to(dt).cuda()
+    kc, vc = _cache(r, B, nh, block, t, dt, hs)
+    pos0 = torch.tensor([t - 1], dtype=torch.int32, device="cuda")
+    y = torch.full((B, nh * hs), float("nan"), device="cuda", dtype=dt)
+    y_lo = torch.full_like(y, float("nan")) if dt == torch.bfloat16 else None
+    G.gpt_attention_decode(q, kc, vc, pos0, splits, y, y_lo)
+    _ok()
+    ref = og.attention(_f64(q), _f64(kc[:, :, :t]), _f64(vc[:, :, :t]), q_pos0=t - 1).reshape(B, nh * hs)
+    if dt == torch.bfloat16:
+        assert np.max(np.abs(_f64(y) - ref)) < 1e-2
+        assert np.max(np.abs(_f64(y) + _f64(y_lo) - ref)) < 2e-5
+    else:
+        assert np.max(np.abs(_f64(y) - ref)) < 2e-5
+
+
+def test_attention_decode_splits_agree():
+    r = _rng(9)
+    q = torch.from_numpy(r.standard_normal((2, 3, 1, 64)).astype(np.float32)).to(torch.bfloat16).cuda()
+    kc, vc = _cache(r, 2, 3, 512, 500, torch.bfloat16)
+    pos0 = torch.tensor([499], dtype=torch.int32, device="cuda")
+    ys = []
+    for s in (1, 2, 5, 31):
+        y = torch.empty(2, 192, device="cuda", dtype=torch.bfloat16)
+        lo = torch.empty_like(y)
+        G.gpt_attention_decode(q, kc, vc, pos0, s, y, lo)
+        ys.append(_f64(y) + _f64(lo))
+    _ok()
+    for y in ys[1:]:
+        assert np.max(np.abs(y - ys[0])) < 1e-5
+
+
+# ------------------------------------------------------------------ sampler (bit-exact)
+
+
+def _run_sampler(logits, T, k, seed, step):
+    B, V = logits.shape
+    ld = torch.from_numpy(logits).cuda()
+    tok = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    thr = torch.empty(B, device="cuda")
+    w = torch.empty(B, V, dtype=torch.int64, device="cuda")
+    G.gpt_sample(ld, T, k, seed, step, tok, thr, w)
+    _ok()
+    return tok.cpu().numpy(), thr.cpu().numpy(), w.cpu().numpy().view(np.uint64)
+
+
+@pytest.mark.parametrize("B,V,T,k", [(1, 65, 0.8, 200), (3, 1000, 1.0, 50), (2, 50304, 1.0, 50),
+                                     (4, 50257, 0.7, 200), (64, 50304, 1.0, 50), (2, 4096, 1.3, 0),
+                                     (2, 5000, 1.0, 1), (1, 50304, 0.9, 4999)])
+def test_sampler_bit_exact_with_oracle(B, V, T, k):
+    for trial in range(3):
+        logits = syn.make_logits(B, V, seed=V + trial, std=2.0)
+        seed, step = 1234 + trial, 7 * trial
+        tok, thr, w = _run_sampler(logits, T, k, seed, step)
+        for b in range(B):
+            s = osm.scaled_logits(logits[b], T)
+            keep = osm.survivors(s, k)
+            w_ref = osm.integer_weights(s, keep)
+            assert np.array_equal(w[b], w_ref), (b, np.flatnonzero(w[b] != w_ref)[:5])
+            assert thr[b] == osm.topk_threshold(s, k)
+            assert tok[b] == osm.sample_row(logits[b], T, k, seed, b, step)
+
+
+def test_sampler_ties_at_threshold_and_greedy():
+    logits = np.zeros((2, 300), np.float32)
+    logits[:, 10:20] = 5.0  # ten-way tie for the top
+    logits[1, 250] = 9.0
+    for step in range(20):
+        tok, thr, w = _run_sampler(logits, 1.0, 3, 5, step)
+        assert 10 <= tok[0] < 20 and (w[0] > 0).sum() == 10  # all ten ties survive k=3
+        assert (w[1] > 0).sum() == 11 and (tok[1] == 250 or 10 <= tok[1] < 20)
+        for b in range(2):
+            assert tok[b] == osm.sample_row(logits[b], 1.0, 3, 5, b, step)
+    tok, _, _ = _run_sampler(logits, 0.0, 0, 0, 0)
+    assert tok.tolist() == [10, 250]
+
+
+def test_sampler_draws_follow_softmax():
+    # many rows of the same logits: each row has its own Philox key
+    V, B = 16, 1024
+    base = np.linspace(-2, 2, V).astype(np.float32)
+    p = np.exp(base.astype(np.float64) - float(base.max()))
+    p /= p.sum()
+    logits = np.tile(base, (B, 1))
+    counts = np.zeros(V)
+    for step in range(20):
+        tok, _, _ = _run_sampler(logits, 1.0, 0, 99, step)
+        counts += np.bincount(tok, minlength=V)
+    from scipy import stats
+    assert stats.chisquare(counts, counts.sum() * p).pvalue > 1e-4
