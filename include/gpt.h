@@ -45,6 +45,7 @@ extern "C" {
 #define GPT_EPOSITION (-7)    /* a kernel saw a position >= block_size                  */
 #define GPT_EUNSUPPORTED (-8) /* device is not sm_103, or a driver entry point is missing */
 #define GPT_ESTATE (-9)       /* call out of order (e.g. decode before prefill)         */
+#define GPT_ETOOBIG (-10)     /* request larger than gpt_attention_decode_noalloc's fixed scratch */
 
 /* ------------------------------------------------------------------ types */
 #define GPT_DTYPE_F32 0  /* weights, activations and cache in fp32 (exact fp32 kernels) */
@@ -205,6 +206,31 @@ int gpt_sample(const float* logits, int32_t B, int32_t V, float temperature, int
 /* Synchronise the current device, then read and clear the stand-alone operations' error
  * word (codes as gpt_sync_status). */
 int gpt_op_status(void);
+
+/* gpt_attention_decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a deployment variant, not a step of the method.
+ *
+ * Who needs it: a process whose device memory is owned by another allocator (a framework's
+ * caching pool, a fixed per-tenant budget) and code that must not call cudaMalloc, which can
+ * block on the device or be forbidden where the caller runs.  This call never allocates:
+ * no cudaMalloc, cudaFree or allocating library routine.  Its split partials and merge
+ * tickets live in one fixed 4 MiB array in device memory that the library keeps on every GPU
+ * that loads it, until the process exits.
+ *
+ * Arguments and results are those of gpt_attention_decode, plus err_dev (dev, int32) or NULL:
+ * error bits the kernel finds (a position at or beyond block) are OR-ed into *err_dev, in the
+ * bit layout gpt_sync_status decodes (4 = position); with NULL they are dropped.
+ * Limits: B * n_head <= 16384, and when splits > 1, B * n_head * splits * (head_size + 2) * 4
+ * bytes must fit in 4 MiB minus 64 KiB; larger requests return GPT_ETOOBIG before anything is
+ * enqueued (gpt_last_error_detail() gives the sizes).
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Every call shares the
+ * array, which keeps the previous call's contents: the call clears the tickets it uses (an
+ * asynchronous memset on `stream`), and calls whose kernels overlap on the same GPU (for
+ * example on two streams) race on the array: the caller must serialise them. */
+int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
+                                 int32_t n_head, int32_t head_size, int32_t block, const int32_t* pos0_dev,
+                                 int32_t splits, void* y, void* y_lo, int32_t* err_dev, void* stream);
 
 #ifdef __cplusplus
 }

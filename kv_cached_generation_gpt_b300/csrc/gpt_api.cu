@@ -746,6 +746,7 @@ const char* gpt_strerror(int code) {
     case GPT_EPOSITION: return "position beyond block_size";
     case GPT_EUNSUPPORTED: return "unsupported device or driver";
     case GPT_ESTATE: return "call out of order";
+    case GPT_ETOOBIG: return "request exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown error";
   }
 }
@@ -1049,6 +1050,92 @@ int gpt_op_status(void) {
   const int zero = 0;
   CK(cudaMemcpy(c->err, &zero, sizeof(int), cudaMemcpyHostToDevice));
   return map_error_word(w);
+}
+
+// ------------------------------------------------------------------ decode attention without allocation
+//
+// For callers that must not allocate device memory: a host process whose allocator owns
+// all of the GPU's memory (a framework's caching pool, a fixed budget in an embedded or
+// multi-tenant server), or code that runs where cudaMalloc is not allowed or would stall
+// the device.  The split-KV partial results and merge tickets of this variant live in one
+// fixed array in device memory that the library holds for as long as it is loaded.
+
+}  // extern "C"
+
+namespace {
+
+// Layout of the fixed scratch: [error word | pad to 256 B][tickets][split partials].
+constexpr size_t NOALLOC_SCRATCH_BYTES = 4u << 20;  // 4 MiB on every GPU that loads the library
+constexpr size_t NOALLOC_TICKET_OFFSET = 256;
+constexpr size_t NOALLOC_MAX_PAIRS = 16384;  // batch x heads
+constexpr size_t NOALLOC_PARTIAL_OFFSET = NOALLOC_TICKET_OFFSET + NOALLOC_MAX_PAIRS * sizeof(unsigned int);
+constexpr size_t NOALLOC_PARTIAL_BYTES = NOALLOC_SCRATCH_BYTES - NOALLOC_PARTIAL_OFFSET;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch per device, looked up once with that device current.
+unsigned char* g_noalloc_addr[64] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(unsigned char** out) {
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return GPT_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    CK(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    g_noalloc_addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return GPT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
+                                 int32_t n_head, int32_t head_size, int32_t block, const int32_t* pos0_dev,
+                                 int32_t splits, void* y, void* y_lo, int32_t* err_dev, void* stream) {
+  if (!q || !k_cache || !v_cache || !y || !pos0_dev || B < 1 || n_head < 1 || block < 1 || splits < 1 ||
+      splits > 1024)
+    return GPT_EINVAL;
+  if (head_size != 64 && head_size != 32) return GPT_EINVAL;
+  if (dtype != GPT_DTYPE_BF16 && dtype != GPT_DTYPE_F32) return GPT_EINVAL;
+  if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;
+  const size_t pairs = static_cast<size_t>(B) * n_head;
+  const size_t partial_bytes = pairs * splits * (head_size + 2) * sizeof(float);
+  if (pairs > NOALLOC_MAX_PAIRS || (splits > 1 && partial_bytes > NOALLOC_PARTIAL_BYTES)) {
+    g_detail = "gpt_attention_decode_noalloc: batch*heads = " + std::to_string(pairs) + " (max " +
+               std::to_string(NOALLOC_MAX_PAIRS) + "), split partials " + std::to_string(partial_bytes) +
+               " bytes (max " + std::to_string(NOALLOC_PARTIAL_BYTES) + ")";
+    return GPT_ETOOBIG;
+  }
+  unsigned char* base = nullptr;
+  int rc = noalloc_scratch(&base);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int* tickets = reinterpret_cast<unsigned int*>(base + NOALLOC_TICKET_OFFSET);
+  float* ws = reinterpret_cast<float*>(base + NOALLOC_PARTIAL_OFFSET);
+  int* err = err_dev ? err_dev : reinterpret_cast<int*>(base);
+  // The array keeps whatever the previous call left: the merge tickets must start at zero.
+  if (splits > 1) CK(cudaMemsetAsync(tickets, 0, pairs * sizeof(unsigned int), st));
+  const int C = head_size * n_head;
+  const dim3 grid(B * n_head, splits);
+  if (dtype == GPT_DTYPE_BF16) {
+    auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
+    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
+                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, ws, tickets,
+                                       static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, err);
+  } else {
+    auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
+    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
+                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, ws, tickets,
+                                       static_cast<float*>(y), nullptr, C, err);
+  }
+  CK(cudaGetLastError());
+  return GPT_OK;
 }
 
 }  // extern "C"

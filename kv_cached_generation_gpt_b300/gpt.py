@@ -24,6 +24,7 @@ GPT_ETIMEOUT = -6
 GPT_EPOSITION = -7
 GPT_EUNSUPPORTED = -8
 GPT_ESTATE = -9
+GPT_ETOOBIG = -10
 
 GPT_DTYPE_F32 = 0
 GPT_DTYPE_BF16 = 1
@@ -32,6 +33,7 @@ EXPORTED = (
     "gpt_create", "gpt_destroy", "gpt_prefill", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
     "gpt_cache_length", "gpt_kernel_launches", "gpt_sync_status", "gpt_strerror", "gpt_last_error_detail", "gpt_linear_bf16",
     "gpt_layernorm", "gpt_attention_prefill", "gpt_attention_decode", "gpt_sample", "gpt_op_status",
+    "gpt_attention_decode_noalloc",
 )
 
 c_int32, c_void_p, c_float, c_uint64, c_int64 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float, ctypes.c_uint64, ctypes.c_int64
@@ -64,7 +66,7 @@ class GptError(RuntimeError):
         self.code = code
         detail = lib().gpt_last_error_detail().decode()
         msg = f"{where}: {lib().gpt_strerror(code).decode()} ({code})"
-        super().__init__(msg + (f" [{detail}]" if detail and code in (GPT_ECUDA, GPT_ENOMEM, GPT_EUNSUPPORTED) else ""))
+        super().__init__(msg + (f" [{detail}]" if detail and code in (GPT_ECUDA, GPT_ENOMEM, GPT_EUNSUPPORTED, GPT_ETOOBIG) else ""))
 
 
 _lib = None
@@ -102,6 +104,9 @@ def lib() -> ctypes.CDLL:
             "gpt_sample": (ctypes.c_int, [c_void_p, c_int32, c_int32, c_float, c_int32, c_uint64, c_int32, c_void_p,
                                           c_void_p, c_void_p, c_void_p]),
             "gpt_op_status": (ctypes.c_int, []),
+            "gpt_attention_decode_noalloc": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                                            c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
+                                                            c_void_p, c_void_p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -238,6 +243,17 @@ def gpt_sample(logits: torch.Tensor, temperature: float, top_k: int | None, seed
 
 def gpt_op_status() -> int:
     return lib().gpt_op_status()
+
+
+def gpt_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pos0: torch.Tensor,
+                                 splits: int, y: torch.Tensor, y_lo: torch.Tensor | None = None,
+                                 err: torch.Tensor | None = None) -> None:
+    """gpt_attention_decode with its scratch in the library's fixed device array (no allocation)."""
+    B, nh, hs = q.shape[0], q.shape[1], q.shape[-1]
+    block = k_cache.shape[2]
+    _check(lib().gpt_attention_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype_code(q.dtype), B, nh, hs,
+                                              block, _ptr(pos0), splits, _ptr(y), _ptr(y_lo), _ptr(err), _stream()),
+           "gpt_attention_decode_noalloc")
 
 
 # ------------------------------------------------------------------ convenience wrapper
