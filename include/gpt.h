@@ -169,6 +169,18 @@ const char* gpt_last_error_detail(void);
 int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
                     int32_t K, int32_t hilo, int32_t block_n, int32_t splits, void* stream);
 
+/* The decode-step Linear kernel: out (dev, fp32, M x N, row stride N) = A W^T (+ bias) for
+ * 1 <= M <= 128 token rows given as a hi/lo pair.  A (dev, bf16): 2M x K, rows [0,M) = hi,
+ * [M,2M) = lo parts of one operand, both multiplied into the same fp32 accumulator.  W (dev,
+ * bf16): N x K (nn.Linear layout).  bias (dev, fp32, N) or NULL.  K % 64 == 0, N >= 1.
+ * The weight rows are the tensor core's 128-row side; each 128-row tile's K range is split
+ * over the CTAs of one thread-block cluster and reduced in split order through distributed
+ * shared memory (deterministic, no scratch memory).  splits: 0 = chosen by the library, else
+ * a power of two <= 16 and <= K/64 (16 needs 16-CTA clusters: GPT_EUNSUPPORTED where the
+ * device cannot schedule them). */
+int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
+                           int32_t K, int32_t splits, void* stream);
+
 /* y (dev, dtype, rows x C) = LayerNorm(x) with eps 1e-5 and biased variance.
  * x (dev, fp32) row r at x + r * x_stride; gamma (dev, fp32, C); beta (dev, fp32, C) or NULL.
  * y_lo (dev, bf16) or NULL: receives y - bf16(y) (only with dtype == GPT_DTYPE_BF16).

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
   const int bh = blockIdx.x, split = blockIdx.y, splits = gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = lane % LPK, g = lane / LPK;
+  griddep_wait();  // q and the new key/value come from the previous kernel
+  griddep_launch();
   const int t_len = *pos0 + 1;
   if (t_len > block) {
     if (threadIdx.x == 0) atomicOr(err, ERR_POSITION);

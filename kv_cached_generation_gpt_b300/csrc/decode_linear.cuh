@@ -1,0 +1,308 @@
+// Linear layers of a decode step: out[b, n] = sum_k a[b, k] W[n, k] (+ fused epilogue) for
+// up to 128 new tokens b, with the activation given as a hi/lo pair of bf16 rows
+// (a = hi + lo; hi rows 0..M-1, lo rows M..2M-1).
+//
+// These are the same four per-layer Linear layers and the tied lm_head as in gemm.cuh
+// ("nanoGPT 架构分析", wangbinyq.github.io, §4.1), at the shapes a KV-cached step gives them:
+// one new row per sequence ("原生 nanoGPT 模型服务首选", §"一个值得做的改进": only the new
+// token is fed), so the work is a stream over the weights with very few rows.
+//
+// Swap-AB on tcgen05: the weight rows (output features) are the MMA's M = 128 side and the
+// token rows its N side, hi rows then lo rows (N = 2 * Bp, Bp = M rounded up to 8).  One
+// 128-feature tile is split along K across the S CTAs of a thread-block cluster (S <= 16).
+// CTA r owns features [r*128/S, (r+1)*128/S) of the tile.  Each CTA adds the hi and lo
+// halves of its fp32 partial, parks it in shared memory grouped by owner, and after one
+// cluster barrier sends each owner its slice with a bulk shared-to-shared copy (TMA engine,
+// completion counted on the owner's mbarrier).  The owner sums the S slices in split order
+// -- a fixed order, so results do not depend on timing -- and applies the epilogue.  No
+// global scratch is used.
+//
+// Programmatic dependent launch: weight tiles do not depend on earlier kernels, so they are
+// requested before griddepcontrol.wait; activations, residual and outputs come after it.
+#pragma once
+
+#include "common.cuh"
+#include "gemm.cuh"
+
+namespace kvgpt {
+
+constexpr int DL_THREADS = 192;  // warps 0-3: TMEM -> partial; warp 4: TMA; warp 5: MMA; all: reduce
+constexpr int DL_MAX_STAGES = 3;
+constexpr int DL_MAX_ROWS = 128;
+constexpr int DL_MAX_SPLITS = 16;
+constexpr uint32_t DL_W_BYTES = 128u * TC_BK * 2u;
+
+__host__ __device__ constexpr int dl_bp(int rows) { return (rows + 7) & ~7; }
+__host__ __device__ constexpr uint32_t dl_stage_bytes(int bp) { return DL_W_BYTES + 2u * bp * 128u; }
+// Once the MMAs are done the ring holds the parked partial, S owner slices of bp x R floats
+// each followed by R floats of padding (bp + 1 rows of 128 floats in all), then the receive
+// slots, S x bp x R floats.
+__host__ __device__ constexpr uint32_t dl_park_bytes(int bp) { return static_cast<uint32_t>((bp + 1) * 512); }
+__host__ __device__ constexpr uint32_t dl_ring_bytes(int bp, int stages) {
+  return stages * dl_stage_bytes(bp) > dl_park_bytes(bp) + static_cast<uint32_t>(bp * 512)
+             ? stages * dl_stage_bytes(bp)
+             : dl_park_bytes(bp) + static_cast<uint32_t>(bp * 512);
+}
+__host__ __device__ constexpr uint32_t dl_smem_bytes(int bp, int stages) {
+  return 1024u + dl_ring_bytes(bp, stages) + 256u;
+}
+
+// Apply the epilogue to 8 consecutive features n0..n0+7 of token row r (n0 % 8 == 0); qpos is
+// the position of the new token (EPI_QKV).
+template <int EPI>
+__device__ __forceinline__ void dl_epilogue8(const Epi<__nv_bfloat16>& e, int r, int n0, float (&v)[8], int qpos) {
+  if (EPI == EPI_F32) {
+    float* dst = e.x + static_cast<size_t>(r) * e.ldx + n0;
+    if (n0 + 8 <= e.N && (e.ldx & 3) == 0) {
+      if (e.bias) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] += e.bias[n0 + j];
+      }
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      for (int j = 0; j < 8 && n0 + j < e.N; ++j) dst[j] = v[j] + (e.bias ? e.bias[n0 + j] : 0.0f);
+    }
+    return;
+  }
+  if (e.bias) {
+    const float4 b0 = reinterpret_cast<const float4*>(e.bias + n0)[0];
+    const float4 b1 = reinterpret_cast<const float4*>(e.bias + n0)[1];
+    v[0] += b0.x; v[1] += b0.y; v[2] += b0.z; v[3] += b0.w;
+    v[4] += b1.x; v[5] += b1.y; v[6] += b1.z; v[7] += b1.w;
+  }
+  if (EPI == EPI_RESID) {
+    float4* dst = reinterpret_cast<float4*>(e.x + static_cast<size_t>(r) * e.ldx + n0);
+    const float4 o0 = dst[0], o1 = dst[1];
+    dst[0] = make_float4(v[0] + o0.x, v[1] + o0.y, v[2] + o0.z, v[3] + o0.w);
+    dst[1] = make_float4(v[4] + o1.x, v[5] + o1.y, v[6] + o1.z, v[7] + o1.w);
+  } else if (EPI == EPI_GELU) {
+    uint4 hi, lo;
+    float g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) g[j] = gelu_erf(v[j]);
+    hi.x = pack_bf16x2(g[0], g[1]);
+    hi.y = pack_bf16x2(g[2], g[3]);
+    hi.z = pack_bf16x2(g[4], g[5]);
+    hi.w = pack_bf16x2(g[6], g[7]);
+    const size_t off = static_cast<size_t>(r) * e.ldo + n0;
+    *reinterpret_cast<uint4*>(e.out + off) = hi;
+    if (e.out_lo) {
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&hi);
+      float l[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) l[j] = g[j] - __bfloat162float(h[j]);
+      lo.x = pack_bf16x2(l[0], l[1]);
+      lo.y = pack_bf16x2(l[2], l[3]);
+      lo.z = pack_bf16x2(l[4], l[5]);
+      lo.w = pack_bf16x2(l[6], l[7]);
+      *reinterpret_cast<uint4*>(e.out_lo + off) = lo;
+    }
+  } else if (EPI == EPI_QKV) {
+    // one new token per sequence: row r is sequence r, at position *pos0
+    const int part = n0 / e.C;
+    const int hn = n0 - part * e.C;
+    const int h = hn / e.hs, d0 = hn - h * e.hs;
+    __nv_bfloat16* dst;
+    if (part == 0) {
+      dst = e.q + (static_cast<size_t>(r) * e.nh + h) * e.hs + d0;
+    } else {
+      const int pos = qpos;  // the cache length before this token (read once per thread)
+      if (pos >= e.block) {
+        atomicOr(e.err, ERR_POSITION);
+        return;
+      }
+      __nv_bfloat16* base = part == 1 ? e.kc : e.vc;
+      dst = base + ((static_cast<size_t>(r) * e.nh + h) * e.block + pos) * e.hs + d0;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(v[0], v[1]);
+    o.y = pack_bf16x2(v[2], v[3]);
+    o.z = pack_bf16x2(v[4], v[5]);
+    o.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+}
+
+// grid.x = n_tiles * splits, cluster (splits, 1, 1); CTA rank r of cluster c works on
+// feature tile c and k-blocks [r*kb_total/splits, (r+1)*kb_total/splits) (splits <= kb_total),
+// through a ring of `stages` (1..3) shared-memory stages.
+// e.M = token rows (<= 128), e.N = output features.
+template <int EPI>
+__global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                 const __grid_constant__ CUtensorMap tmX,
+                                                                 int kb_total, int splits, int stages,
+                                                                 Epi<__nv_bfloat16> e) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int bp = dl_bp(e.M);
+  const uint32_t stage_bytes = dl_stage_bytes(bp);
+  const uint32_t x_bytes = 2u * bp * 128u;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + dl_ring_bytes(bp, stages));
+  uint64_t* empty = full + DL_MAX_STAGES;
+  uint64_t* acc_full = empty + DL_MAX_STAGES;
+  uint64_t* recv_full = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_full + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int tile = blockIdx.x / splits;
+  const int kb0 = (rank * kb_total) / splits, kb1 = ((rank + 1) * kb_total) / splits;
+  const int nkb = kb1 - kb0;
+  const int R = 128 / splits;                  // features owned by each CTA of the cluster
+  const int slice = (bp + 1) * R;              // floats per owner slice in the parked partial
+  const uint32_t slice_bytes = static_cast<uint32_t>(bp * R * 4);
+  float* park = reinterpret_cast<float*>(smem);
+  float* recv = reinterpret_cast<float*>(smem + dl_park_bytes(bp));  // [S][bp][R]
+  uint32_t tcols = 32;
+  while (tcols < static_cast<uint32_t>(2 * bp)) tcols <<= 1;
+
+  auto w_tile = [&](int s) { return smem + s * stage_bytes; };
+  auto x_tile = [&](int s) { return smem + s * stage_bytes + DL_W_BYTES; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(recv_full, 1);
+    fence_mbar_init();
+    // the S - 1 peers' slices for this CTA complete on recv_full
+    if (splits > 1) mbar_arrive_expect_tx(recv_full, static_cast<uint32_t>(splits - 1) * slice_bytes);
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_launch();  // this CTA holds its TMEM: the next kernel may begin its own prologue
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmW);
+      tma_prefetch_desc(&tmX);
+      const int pre = min(nkb, stages);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], DL_W_BYTES + x_bytes);
+        tma_load_2d(&tmW, &full[i], w_tile(i), (kb0 + i) * TC_BK, tile * 128);
+      }
+      griddep_wait();  // activations come from the previous kernel
+      for (int i = 0; i < pre; ++i) {
+        tma_load_2d(&tmX, &full[i], x_tile(i), (kb0 + i) * TC_BK, 0);
+        tma_load_2d(&tmX, &full[i], x_tile(i) + bp * 128, (kb0 + i) * TC_BK, e.M);
+      }
+      int issued = pre;
+      for (int i = pre; i < nkb; ++i) {
+        const int s = i % stages;
+        if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, e.err)) break;
+        mbar_arrive_expect_tx(&full[s], DL_W_BYTES + x_bytes);
+        const int kx = (kb0 + i) * TC_BK;
+        tma_load_2d(&tmW, &full[s], w_tile(s), kx, tile * 128);
+        tma_load_2d(&tmX, &full[s], x_tile(s), kx, 0);
+        tma_load_2d(&tmX, &full[s], x_tile(s) + bp * 128, kx, e.M);
+        issued = i + 1;
+      }
+      // Drain: the most recent load into each stage has landed before shared memory is reused.
+      for (int i = max(0, issued - stages); i < issued; ++i) mbar_wait(&full[i % stages], (i / stages) & 1, e.err);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 2 * bp);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % stages;
+        if (!mbar_wait(&full[s], (i / stages) & 1, e.err)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(w_tile(s)), b0 = smem_u32(x_tile(s));
+#pragma unroll
+        for (int k = 0; k < TC_BK / 16; ++k)
+          umma_bf16(tmem, sdesc_sw128(a0 + 32 * k), sdesc_sw128(b0 + 32 * k), idesc, (i | k) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(acc_full);
+      mbar_wait(acc_full, 0, e.err);  // no MMA in flight once this returns
+    }
+  } else {
+    // Warps 0-3: TMEM lane f = feature f of the tile.  Park hi + lo at park[o][row][f % R] of
+    // owner o = f / R, in the ring: every load into it has landed and every MMA reading it
+    // has completed.
+    const bool ok = mbar_wait(acc_full, 0, e.err);
+    tc_fence_after();
+    const int f = warp * 32 + lane;
+    float* dst = park + (f / R) * slice + (f % R);
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < bp; c += 16) {
+      uint32_t hi[16], lo[16];
+      const bool two = c + 8 < bp;  // bp is a multiple of 8: 16 columns, or the last 8
+      if (two) {
+        tmem_ld16_raw(t_row + c, hi);
+        tmem_ld16_raw(t_row + bp + c, lo);
+      } else {
+        tmem_ld8_raw(t_row + c, hi);
+        tmem_ld8_raw(t_row + bp + c, lo);
+      }
+      tmem_wait_ld16(hi, lo);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < 8 || two) dst[(c + j) * R] = ok ? __uint_as_float(hi[j]) + __uint_as_float(lo[j]) : 0.0f;
+    }
+    fence_proxy_async_smem();  // the parked partial is read by bulk copies (async proxy)
+  }
+  __syncwarp();
+  tc_fence_before();
+  if (splits > 1) {
+    // Every CTA of the cluster has finished with its ring: its receive slots may be written.
+    cluster_sync();
+    if (threadIdx.x == 0) {
+      for (int o = 1; o < splits; ++o) {
+        const int to = (rank + o) % splits;
+        const uint32_t dst = mapa_shared(smem_u32(recv + rank * bp * R), static_cast<uint32_t>(to));
+        const uint32_t bar = mapa_shared(smem_u32(recv_full), static_cast<uint32_t>(to));
+        bulk_copy_s2cluster(dst, smem_u32(park + to * slice), slice_bytes, bar);
+      }
+      bulk_commit();
+    }
+    mbar_wait(recv_full, 0, e.err);
+  } else {
+    __syncthreads();
+  }
+
+  // Reduce: this CTA's R features of the tile, for every token row, in split order.
+  griddep_wait();
+  const int upr = R / 8;
+  const int units = e.M * upr;
+  int qpos = 0;
+  if (EPI == EPI_QKV && e.pos0) qpos = *e.pos0;
+#pragma unroll 1
+  for (int u = threadIdx.x; u < units; u += DL_THREADS) {
+    const int r = u / upr;
+    const int fl = (u - r * upr) * 8;
+    const int n0 = tile * 128 + rank * R + fl;
+    if (n0 >= e.N) continue;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+#pragma unroll 1
+    for (int s = 0; s < splits; ++s) {
+      const float* src = s == rank ? park + rank * slice + r * R + fl : recv + (s * bp + r) * R + fl;
+      const float4 p0 = reinterpret_cast<const float4*>(src)[0];
+      const float4 p1 = reinterpret_cast<const float4*>(src)[1];
+      v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+      v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+    }
+    dl_epilogue8<EPI>(e, r, n0, v, qpos);
+  }
+  // The bulk copies out of this CTA's shared memory must have read it before the CTA exits.
+  if (splits > 1 && threadIdx.x == 0) bulk_wait_read();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+}
+
+}  // namespace kvgpt

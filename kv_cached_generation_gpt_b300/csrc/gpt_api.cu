@@ -26,6 +26,7 @@
 #include "../../include/gpt.h"
 #include "attention.cuh"
 #include "common.cuh"
+#include "decode_linear.cuh"
 #include "gemm.cuh"
 #include "norm.cuh"
 #include "sampler.cuh"
@@ -177,6 +178,138 @@ cudaError_t set_tc_attr(int bn, bool hilo, int epi, int dev) {
   return cudaErrorInvalidValue;
 }
 
+// ------------------------------------------------------------------ decode-shape linear layers
+
+// Per device: how many clusters of the decode linear kernel can be resident at once, for
+// each cluster size (2, 4, 8, 16), token-row class (bp = 8 .. 128) and stage count (1 .. 3).
+// Filled once per device (outside any stream capture); plans keep a launch within one wave.
+int g_dl_max_clusters[64][5][DL_MAX_ROWS / 8][DL_MAX_STAGES] = {};
+unsigned long long g_dl_attr_mask = 0;
+std::mutex g_dl_mu;
+
+template <int EPI>
+cudaError_t dl_attr() {
+  auto kern = dec_linear_kernel<EPI>;
+  cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(dl_smem_bytes(DL_MAX_ROWS, DL_MAX_STAGES)));
+  if (r != cudaSuccess) return r;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+int dl_max_clusters(int dev, int splits, int bp, int stages) {
+  int si = 0;
+  while ((2 << si) < splits) ++si;
+  return g_dl_max_clusters[dev][si][bp / 8 - 1][stages - 1];
+}
+
+cudaError_t init_dl_attrs(int dev) {
+  std::lock_guard<std::mutex> lk(g_dl_mu);
+  if (g_dl_attr_mask & (1ull << dev)) return cudaSuccess;
+  cudaError_t r;
+  if ((r = dl_attr<EPI_F32>()) != cudaSuccess) return r;
+  if ((r = dl_attr<EPI_RESID>()) != cudaSuccess) return r;
+  if ((r = dl_attr<EPI_GELU>()) != cudaSuccess) return r;
+  if ((r = dl_attr<EPI_QKV>()) != cudaSuccess) return r;
+  for (int si = 0; si < 5; ++si)
+    for (int bi = 0; bi < DL_MAX_ROWS / 8; ++bi)
+      for (int st = 1; st <= DL_MAX_STAGES; ++st) {
+        const int splits = 2 << si;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(splits * 16);
+        cfg.blockDim = dim3(DL_THREADS);
+        cfg.dynamicSmemBytes = dl_smem_bytes(8 * (bi + 1), st);
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = splits;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (splits > DL_MAX_SPLITS || cudaOccupancyMaxActiveClusters(&n, dec_linear_kernel<EPI_RESID>, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          n = 0;
+        }
+        g_dl_max_clusters[dev][si][bi][st - 1] = n;
+      }
+  g_dl_attr_mask |= 1ull << dev;
+  return cudaSuccess;
+}
+
+int dl_stages(int kb, int splits) { return std::min(DL_MAX_STAGES, cdiv(kb, splits)); }
+
+// Split-K factor (= cluster size): the largest power of two <= 16 and <= the k-block count
+// that keeps the grid within 2/3 of the SMs and all clusters resident in one wave.  (Fewer,
+// larger CTAs measure faster than one CTA per SM here: the cost is latency, not bandwidth.)
+int plan_dl_splits(int n_tiles, int kb, int rows, int num_sms, int dev) {
+  const int bp = dl_bp(rows);
+  int s = 1;
+  for (int c = 2; c <= DL_MAX_SPLITS && c <= kb; c *= 2) {
+    if (static_cast<long long>(n_tiles) * c * 3 > 2LL * num_sms) break;
+    if (dl_max_clusters(dev, c, bp, dl_stages(kb, c)) < n_tiles) break;
+    s = c;
+  }
+  return s;
+}
+
+cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+// Launch `kern` on `st`, as a programmatic dependent of the previous kernel when pdl is set
+// (the kernel must call griddep_wait before touching data that earlier kernels produce).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <int EPI>
+cudaError_t launch_dl_epi(const CUtensorMap& tw, const CUtensorMap& tx, int kb, int splits, int n_tiles,
+                          const Epi<bf16>& e, bool pdl, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  const int stages = dl_stages(kb, splits);
+  cfg.gridDim = dim3(n_tiles * splits);
+  cfg.blockDim = dim3(DL_THREADS);
+  cfg.dynamicSmemBytes = dl_smem_bytes(dl_bp(e.M), stages);
+  cfg.stream = st;
+  if (splits > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = splits;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) attr[na++] = pdl_attr();
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, dec_linear_kernel<EPI>, tw, tx, kb, splits, stages, e);
+}
+
+cudaError_t launch_dl(int epi, const CUtensorMap& tw, const CUtensorMap& tx, int kb, int splits, int n_tiles,
+                      const Epi<bf16>& e, bool pdl, cudaStream_t st) {
+  switch (epi) {
+    case EPI_F32: return launch_dl_epi<EPI_F32>(tw, tx, kb, splits, n_tiles, e, pdl, st);
+    case EPI_RESID: return launch_dl_epi<EPI_RESID>(tw, tx, kb, splits, n_tiles, e, pdl, st);
+    case EPI_GELU: return launch_dl_epi<EPI_GELU>(tw, tx, kb, splits, n_tiles, e, pdl, st);
+    case EPI_QKV: return launch_dl_epi<EPI_QKV>(tw, tx, kb, splits, n_tiles, e, pdl, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 // Raise the dynamic shared memory limit of every tensor-core GEMM instantiation and of
 // the sampler once per device, before any stream capture can need them.
 cudaError_t init_kernel_attrs(int dev) {
@@ -188,7 +321,7 @@ cudaError_t init_kernel_attrs(int dev) {
         cudaError_t r = set_tc_attr(bns[bi], h != 0, epi, dev);
         if (r != cudaSuccess) return r;
       }
-  return cudaSuccess;
+  return init_dl_attrs(dev);
 }
 
 struct GemmPlan {
@@ -225,6 +358,7 @@ __global__ void set_ints_kernel(int* a, int va, int* b, int vb) {
   if (b) *b = vb;
 }
 __global__ void advance_kernel(int* pos, int* step) {
+  griddep_wait();
   *pos += 1;
   *step += 1;
 }
@@ -236,11 +370,19 @@ int map_error_word(int w) {
   return GPT_OK;
 }
 
+// Candidate slots the sampler gets after the V scaled logits: up to 4096, within the 227 KiB
+// of dynamic shared memory a CTA may have (minus the kernel's static shared memory).
+int sampler_cand_cap(int V) {
+  const long long room = 232448LL - 4096 - static_cast<long long>(V) * 4;
+  return static_cast<int>(std::max(0LL, std::min(4096LL, room / 4)));
+}
+size_t sampler_smem(int V) { return static_cast<size_t>(V + sampler_cand_cap(V)) * 4; }
+
 cudaError_t set_sampler_smem(int dev, int V) {
   static int done_bytes[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
-  const int bytes = V * static_cast<int>(sizeof(float));
+  const int bytes = static_cast<int>(sampler_smem(V));
   if (done_bytes[dev] >= bytes) return cudaSuccess;
   cudaError_t r = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (r == cudaSuccess) done_bytes[dev] = bytes;
@@ -420,6 +562,25 @@ int gemm_bf16(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, b
   return GPT_OK;
 }
 
+// Decode-shape Linear (M <= 128 token rows given as a hi/lo pair): swap-AB tcgen05 kernel with
+// cluster split-K, launched as a programmatic dependent of the previous kernel.
+int dec_linear(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, int epi, Epi<bf16> e) {
+  const int kb = K / TC_BK, n_tiles = cdiv(N, 128);
+  const int splits = plan_dl_splits(n_tiles, kb, M, m->num_sms, m->dev);
+  CUtensorMap tx, tw;
+  int rc = make_tmap(&tx, A, 2LL * M, K, dl_bp(M));
+  if (rc) return rc;
+  rc = m->weight_map(W, N, K, 128, &tw);
+  if (rc) return rc;
+  e.M = M;
+  e.N = N;
+  e.T = 1;
+  e.err = m->d_err;
+  CK(launch_dl(epi, tw, tx, kb, splits, n_tiles, e, true, m->stream));
+  ++m->launches;
+  return GPT_OK;
+}
+
 template <int EPI>
 int gemm_f32(gpt_model* m, const float* A, const void* W, int M, int N, int K, Epi<float> e) {
   e.M = M;
@@ -449,6 +610,9 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   constexpr bool kBf16 = std::is_same<TE, bf16>::value;
   const int C = m->C, nh = m->nh, V = m->V, rows = B * T;
   const bool hilo = kBf16 && decode && m->hilo_decode;
+  // decode-shape Linear layers (swap-AB, cluster split-K) and programmatic dependent launches
+  const bool dl = hilo && rows <= DL_MAX_ROWS;
+  const bool pdl = decode;
   const int* pos0 = decode ? m->d_pos : nullptr;
   cudaStream_t st = m->stream;
   TE* xn = static_cast<TE*>(m->xn);
@@ -468,10 +632,9 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     TE* kc = static_cast<TE*>(m->kcache(l));
     TE* vc = static_cast<TE*>(m->vcache(l));
     // ln_1
-    layernorm_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(m->x, rows, C, C, w.ln1_w, w.ln1_b, xn,
-                                                                    hilo ? xn + static_cast<size_t>(rows) * C : nullptr,
-                                                                    C);
-    CK(cudaGetLastError());
+    CK(launch_k(layernorm_kernel<TE>, dim3(cdiv(rows, rows_per_cta)), dim3(256), 0, st, pdl, m->x, rows, C,
+                static_cast<long long>(C), w.ln1_w, w.ln1_b, xn,
+                hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C));
     ++m->launches;
     // c_attn + KV append
     {
@@ -488,7 +651,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.pos0 = pos0;
       int rc;
       if constexpr (kBf16)
-        rc = gemm_bf16(m, xn, w.attn_w, rows, 3 * C, C, hilo, EPI_QKV, e, decode);
+        rc = dl ? dec_linear(m, xn, w.attn_w, rows, 3 * C, C, EPI_QKV, e)
+                : gemm_bf16(m, xn, w.attn_w, rows, 3 * C, C, hilo, EPI_QKV, e, decode);
       else
         rc = gemm_f32<EPI_QKV>(m, xn, w.attn_w, rows, 3 * C, C, e);
       if (rc) return rc;
@@ -497,12 +661,15 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     if (decode) {
       const int splits = decode_attn_splits(m, B);
       TE* y_lo = hilo ? y + static_cast<size_t>(B) * C : nullptr;
+      const TE* qc = q;
       if (m->hs == 64)
-        attn_decode_kernel<TE, 64><<<dim3(B * nh, splits), DEC_THREADS, 0, st>>>(
-            q, kc, vc, nh, m->block, m->d_pos, m->ws, m->tickets, y, y_lo, C, m->d_err);
+        CK(launch_k(attn_decode_kernel<TE, 64>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, pdl, qc,
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
+                    static_cast<const int*>(m->d_pos), m->ws, m->tickets, y, y_lo, C, m->d_err));
       else
-        attn_decode_kernel<TE, 32><<<dim3(B * nh, splits), DEC_THREADS, 0, st>>>(
-            q, kc, vc, nh, m->block, m->d_pos, m->ws, m->tickets, y, y_lo, C, m->d_err);
+        CK(launch_k(attn_decode_kernel<TE, 32>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, pdl, qc,
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
+                    static_cast<const int*>(m->d_pos), m->ws, m->tickets, y, y_lo, C, m->d_err));
     } else if constexpr (kBf16) {
       attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
     } else {
@@ -521,16 +688,16 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.ldx = C;
       int rc;
       if constexpr (kBf16)
-        rc = gemm_bf16(m, y, w.proj_w, rows, C, C, hilo, EPI_RESID, e, decode);
+        rc = dl ? dec_linear(m, y, w.proj_w, rows, C, C, EPI_RESID, e)
+                : gemm_bf16(m, y, w.proj_w, rows, C, C, hilo, EPI_RESID, e, decode);
       else
         rc = gemm_f32<EPI_RESID>(m, y, w.proj_w, rows, C, C, e);
       if (rc) return rc;
     }
     // ln_2
-    layernorm_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(m->x, rows, C, C, w.ln2_w, w.ln2_b, xn,
-                                                                    hilo ? xn + static_cast<size_t>(rows) * C : nullptr,
-                                                                    C);
-    CK(cudaGetLastError());
+    CK(launch_k(layernorm_kernel<TE>, dim3(cdiv(rows, rows_per_cta)), dim3(256), 0, st, pdl, m->x, rows, C,
+                static_cast<long long>(C), w.ln2_w, w.ln2_b, xn,
+                hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C));
     ++m->launches;
     // mlp c_fc + GELU
     {
@@ -541,7 +708,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.ldo = 4 * C;
       int rc;
       if constexpr (kBf16)
-        rc = gemm_bf16(m, xn, w.fc_w, rows, 4 * C, C, hilo, EPI_GELU, e, decode);
+        rc = dl ? dec_linear(m, xn, w.fc_w, rows, 4 * C, C, EPI_GELU, e)
+                : gemm_bf16(m, xn, w.fc_w, rows, 4 * C, C, hilo, EPI_GELU, e, decode);
       else
         rc = gemm_f32<EPI_GELU>(m, xn, w.fc_w, rows, 4 * C, C, e);
       if (rc) return rc;
@@ -554,17 +722,18 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.ldx = C;
       int rc;
       if constexpr (kBf16)
-        rc = gemm_bf16(m, hbuf, w.mproj_w, rows, C, 4 * C, hilo, EPI_RESID, e, decode);
+        rc = dl ? dec_linear(m, hbuf, w.mproj_w, rows, C, 4 * C, EPI_RESID, e)
+                : gemm_bf16(m, hbuf, w.mproj_w, rows, C, 4 * C, hilo, EPI_RESID, e, decode);
       else
         rc = gemm_f32<EPI_RESID>(m, hbuf, w.mproj_w, rows, C, 4 * C, e);
       if (rc) return rc;
     }
   }
   // ln_f on the last position of each sequence, then the tied lm_head
-  layernorm_kernel<TE><<<cdiv(B, rows_per_cta), 256, 0, st>>>(
-      m->x + static_cast<size_t>(T - 1) * C, B, C, static_cast<long long>(T) * C, m->ln_f_w, m->ln_f_b, xf,
-      kBf16 ? xf + static_cast<size_t>(B) * C : nullptr, C);
-  CK(cudaGetLastError());
+  CK(launch_k(layernorm_kernel<TE>, dim3(cdiv(B, rows_per_cta)), dim3(256), 0, st, pdl,
+              static_cast<const float*>(m->x + static_cast<size_t>(T - 1) * C), B, C, static_cast<long long>(T) * C,
+              static_cast<const float*>(m->ln_f_w), static_cast<const float*>(m->ln_f_b), xf,
+              kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C));
   ++m->launches;
   {
     Epi<TE> e;
@@ -572,7 +741,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     e.ldx = V;
     int rc;
     if constexpr (kBf16)
-      rc = gemm_bf16(m, xf, m->wte, B, V, C, true, EPI_F32, e, false);
+      rc = B <= DL_MAX_ROWS ? dec_linear(m, xf, m->wte, B, V, C, EPI_F32, e)
+                            : gemm_bf16(m, xf, m->wte, B, V, C, true, EPI_F32, e, false);
     else
       rc = gemm_f32<EPI_F32>(m, xf, m->wte, B, V, C, e);
     if (rc) return rc;
@@ -603,8 +773,8 @@ int enqueue_sample(gpt_model* m, int B, float temperature, int top_k, unsigned l
   a.next_tokens = m->d_tokens;
   a.thr_out = nullptr;
   a.w_out = nullptr;
-  sample_kernel<<<B, SMP_THREADS, m->V * sizeof(float), st>>>(a);
-  CK(cudaGetLastError());
+  a.cand_cap = sampler_cand_cap(m->V);
+  CK(launch_k(sample_kernel, dim3(B), dim3(SMP_THREADS), sampler_smem(m->V), st, true, a));
   ++m->launches;
   return GPT_OK;
 }
@@ -852,8 +1022,8 @@ int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32
       rc = forward(m, m->d_tokens, B, 1, true, m->logits);
       if (!rc) rc = enqueue_sample(m, B, temperature, top_k, seed, m->d_step, 0, out, W, T, m->cap_stream);
       if (!rc) {
-        advance_kernel<<<1, 1, 0, m->cap_stream>>>(m->d_pos, m->d_step);
-        if (cudaGetLastError() != cudaSuccess) rc = GPT_ECUDA;
+        if (launch_k(advance_kernel, dim3(1), dim3(1), 0, m->cap_stream, true, m->d_pos, m->d_step) != cudaSuccess)
+          rc = GPT_ECUDA;
         ++m->launches;
       }
       m->graph_kernels = m->launches - launches0;
@@ -938,6 +1108,40 @@ int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out,
   e.tickets = c->tickets;
   e.err = c->err;
   CK(dispatch_tc(p.bn, hilo != 0, EPI_F32, dev, ta, tb, M, N, K, p.splits, e, static_cast<cudaStream_t>(stream)));
+  return GPT_OK;
+}
+
+int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
+                           int32_t K, int32_t splits, void* stream) {
+  if (!A || !W || !out || M < 1 || M > DL_MAX_ROWS || N < 1 || K < 64 || K % 64 != 0 || splits < 0) return GPT_EINVAL;
+  const int kb = K / TC_BK;
+  if (splits > 0 && ((splits & (splits - 1)) != 0 || splits > DL_MAX_SPLITS || splits > kb)) return GPT_EINVAL;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return GPT_EUNSUPPORTED;
+  CK(init_dl_attrs(dev));
+  int num_sms = 148;
+  CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  const int n_tiles = cdiv(N, 128);
+  if (splits == 0) splits = plan_dl_splits(n_tiles, kb, M, num_sms, dev);
+  if (splits > 1 && dl_max_clusters(dev, splits, dl_bp(M), dl_stages(kb, splits)) < 1) {
+    g_detail = std::to_string(splits) + "-CTA clusters of this size cannot be scheduled on this device";
+    return GPT_EUNSUPPORTED;
+  }
+  OpCtx* c = nullptr;
+  int rc = op_ctx(&c, 0, 0);
+  if (rc) return rc;
+  CUtensorMap tx, tw;
+  if ((rc = make_tmap(&tx, A, 2LL * M, K, dl_bp(M)))) return rc;
+  if ((rc = make_tmap(&tw, W, N, K, 128))) return rc;
+  Epi<bf16> e;
+  e.M = M;
+  e.N = N;
+  e.bias = bias;
+  e.x = out;
+  e.ldx = N;
+  e.err = c->err;
+  CK(launch_dl(EPI_F32, tw, tx, kb, splits, n_tiles, e, false, static_cast<cudaStream_t>(stream)));
   return GPT_OK;
 }
 
@@ -1035,7 +1239,8 @@ int gpt_sample(const float* logits, int32_t B, int32_t V, float temperature, int
   a.next_tokens = tokens;
   a.thr_out = thresholds;
   a.w_out = reinterpret_cast<unsigned long long*>(weights);
-  sample_kernel<<<B, SMP_THREADS, V * sizeof(float), static_cast<cudaStream_t>(stream)>>>(a);
+  a.cand_cap = sampler_cand_cap(V);
+  sample_kernel<<<B, SMP_THREADS, sampler_smem(V), static_cast<cudaStream_t>(stream)>>>(a);
   CK(cudaGetLastError());
   return GPT_OK;
 }

@@ -18,6 +18,8 @@ template <typename TW>
 __global__ void embed_kernel(const int* __restrict__ tokens, int rows, int T, const int* pos0,
                              const TW* __restrict__ wte, const TW* __restrict__ wpe, int V, int block, int C,
                              float* __restrict__ x, int* err) {
+  griddep_wait();
+  griddep_launch();
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -48,6 +50,8 @@ template <typename TO>
 __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, long long in_stride,
                                  const float* __restrict__ gamma, const float* __restrict__ beta,
                                  TO* __restrict__ y, TO* __restrict__ y_lo, int ldy) {
+  griddep_wait();  // x comes from the previous kernel (a programmatic dependent launch may start early)
+  griddep_launch();
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;

@@ -97,17 +97,161 @@ struct SampleArgs {
   int* next_tokens;        // nullable: next_tokens[b] = token
   float* thr_out;          // nullable: the threshold tau per row (-inf: no top-k)
   unsigned long long* w_out;  // nullable: the integer weights [B][V]
+  int cand_cap;            // candidate slots after the V scaled logits in dynamic shared memory
 };
 
+struct SampleSmem {
+  unsigned int hist[256];
+  float rf[SMP_WARPS];
+  int ri[SMP_WARPS];
+  unsigned long long ru[SMP_WARPS];
+  unsigned int prefix, remaining;
+  unsigned long long target;
+  int flag;
+};
+
+// Block-wide: the k-th largest (1-based, duplicates counted) of n order-preserving keys
+// key_at(0..n-1), by a radix select 8 bits at a time from the top.
+template <typename KeyAt>
+__device__ unsigned int block_select_desc(KeyAt key_at, int n, unsigned int k, SampleSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __syncthreads();
+  if (tid == 0) {
+    sm.prefix = 0u;
+    sm.remaining = k;
+  }
+  unsigned int pmask = 0u;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    if (tid < 256) sm.hist[tid] = 0u;
+    __syncthreads();
+    const unsigned int prefix = sm.prefix;
+    for (int i = tid; i < n; i += SMP_THREADS) {
+      const unsigned int key = key_at(i);
+      const bool cand = (key & pmask) == prefix;
+      const unsigned int dig = (key >> shift) & 255u;
+      // aggregate equal digits within the warp: one shared-memory atomic per distinct digit
+      const unsigned int act = __ballot_sync(__activemask(), cand);
+      if (cand) {
+        const unsigned int peers = __match_any_sync(act, dig);
+        if ((__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[dig], static_cast<unsigned int>(__popc(peers)));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 248-8l (descending); find the bin holding the remaining-th
+      unsigned int c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sm.hist[255 - 8 * lane - j];
+        tot += c[j];
+      }
+      unsigned int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned int rem = sm.remaining;
+      const unsigned int excl = incl - tot;
+      if (excl < rem && rem <= incl) {
+        unsigned int run = excl;
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= rem) {
+            const unsigned int dig = 255u - 8u * lane - j;
+            sm.remaining = rem - run;
+            sm.prefix = prefix | (dig << shift);
+            break;
+          }
+          run += c[j];
+        }
+      }
+    }
+    pmask |= 255u << shift;
+    __syncthreads();
+  }
+  return sm.prefix;
+}
+
+// Block-wide exclusive prefix sum of one uint64 per thread (in thread order); returns the
+// exclusive prefix, and the total in *total.
+__device__ __forceinline__ unsigned long long block_scan_u64(unsigned long long v, unsigned long long* total,
+                                                             SampleSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) sm.ru[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long wt = sm.ru[lane];
+    unsigned long long wi = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    sm.ru[lane] = wi - wt;
+    if (lane == 31) sm.target = wi;  // total, read below before the caller reuses `target`
+  }
+  __syncthreads();
+  *total = sm.target;
+  return sm.ru[warp] + incl - v;
+}
+
+// The draw over items j = 0..n-1 in ascending token order, item j being token idx(j) with
+// scaled logit val(j): integer weights of the survivors (val >= tau), their total W, the
+// target floor(r W / 2^64), and the first item whose running sum exceeds it.  Each thread
+// takes a contiguous run of items so the block scan follows the item order.
+template <typename IdxAt, typename ValAt, typename Emit>
+__device__ void draw_over(int n, IdxAt idx_at, ValAt val_at, float tau, float m, unsigned long long seed, int row,
+                          int step, Emit emit, SampleSmem& sm) {
+  const int tid = threadIdx.x;
+  const int chunk = (n + SMP_THREADS - 1) / SMP_THREADS;
+  const int j0 = min(n, tid * chunk), j1 = min(n, j0 + chunk);
+  unsigned long long local = 0;
+  for (int j = j0; j < j1; ++j) {
+    const float s = val_at(j);
+    local += (s >= tau) ? weight40(s, m) : 0ull;
+  }
+  unsigned long long W = 0;
+  const unsigned long long excl = block_scan_u64(local, &W, sm);
+  const unsigned long long r =
+      philox_word0(seed, static_cast<unsigned long long>(row), static_cast<unsigned long long>(step));
+  const unsigned long long target = __umul64hi(r, W);
+  if (local > 0 && excl <= target && target < excl + local) {
+    unsigned long long run = excl;
+    for (int j = j0; j < j1; ++j) {
+      const float s = val_at(j);
+      run += (s >= tau) ? weight40(s, m) : 0ull;
+      if (run > target) {
+        emit(idx_at(j), tau);
+        break;
+      }
+    }
+  }
+}
+
+// One CTA per row.  Dynamic shared memory: V scaled logits, then cand_cap int slots.
+//
+// The threshold tau (the k'-th largest s) is found without sorting the row: the maxima of
+// 1024 disjoint groups give k' distinct elements >= L, their k'-th largest, so L <= tau and
+// every survivor is a candidate with s >= L.  The candidates (usually a little over k') are
+// compacted in ascending index order, tau is selected among them, and the draw runs over
+// them: non-candidates have s < L <= tau and weight 0, so W and the pick are unchanged.
+// When there are more candidates than slots (heavily tied rows) or k' > 1024, tau is
+// selected over the whole row instead.
 __global__ void __launch_bounds__(SMP_THREADS) sample_kernel(SampleArgs a) {
-  extern __shared__ float s_s[];  // V scaled logits
-  __shared__ unsigned int s_hist[256];
-  __shared__ float s_rf[SMP_WARPS];
-  __shared__ int s_ri[SMP_WARPS];
-  __shared__ unsigned long long s_ru[SMP_WARPS];
-  __shared__ unsigned int s_prefix, s_remaining;
-  __shared__ unsigned long long s_target;
+  extern __shared__ __align__(16) float s_s[];  // V scaled logits, then the candidate slots
+  __shared__ SampleSmem sm;
+  int* s_cand = reinterpret_cast<int*>(s_s + a.V);
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  griddep_wait();  // the logits come from the previous kernel
+  griddep_launch();
   const float* lr = a.logits + static_cast<size_t>(b) * a.ld;
   const int V = a.V;
   const int step = a.step_dev ? *a.step_dev : a.step;
@@ -138,152 +282,120 @@ __global__ void __launch_bounds__(SMP_THREADS) sample_kernel(SampleArgs a) {
       }
     }
     if (lane == 0) {
-      s_rf[warp] = best;
-      s_ri[warp] = bi;
+      sm.rf[warp] = best;
+      sm.ri[warp] = bi;
     }
     __syncthreads();
     if (tid == 0) {
       for (int w = 1; w < SMP_WARPS; ++w)
-        if (s_rf[w] > best || (s_rf[w] == best && s_ri[w] < bi)) {
-          best = s_rf[w];
-          bi = s_ri[w];
+        if (sm.rf[w] > best || (sm.rf[w] == best && sm.ri[w] < bi)) {
+          best = sm.rf[w];
+          bi = sm.ri[w];
         }
       emit(bi == 0x7fffffff ? 0 : bi, -INFINITY);
     }
     return;
   }
 
-  // 1. s = l / T, its maximum and minimum
+  // 1. s = l / T; the row's maximum and minimum, and the maximum of group tid = {i : i % 1024 == tid}
+  //    (16 loads in flight per thread; l / 1 == l exactly, so T = 1 skips the division)
   float mx = -INFINITY, mn = INFINITY;
-  for (int i = tid; i < V; i += SMP_THREADS) {
-    const float s = __fdiv_rn(lr[i], a.temperature);
-    s_s[i] = s;
-    mx = fmaxf(mx, s);
-    mn = fminf(mn, s);
+  const bool unit_t = a.temperature == 1.0f;
+  constexpr int BATCH = 16;
+#pragma unroll 1
+  for (int i0 = tid; i0 < V; i0 += BATCH * SMP_THREADS) {
+    float l[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int i = i0 + u * SMP_THREADS;
+      l[u] = i < V ? __ldg(lr + i) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int i = i0 + u * SMP_THREADS;
+      if (i < V) {
+        const float s = unit_t ? l[u] : __fdiv_rn(l[u], a.temperature);
+        s_s[i] = s;
+        mx = fmaxf(mx, s);
+        mn = fminf(mn, s);
+      }
+    }
   }
+  const float gmax = mx;
   mx = warp_max(mx);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
   if (lane == 0) {
-    s_rf[warp] = mx;
-    s_ri[warp] = __float_as_int(mn);
+    sm.rf[warp] = mx;
+    sm.ri[warp] = __float_as_int(mn);
   }
   __syncthreads();
-  float m = s_rf[0], vmin = __int_as_float(s_ri[0]);
+  float m = sm.rf[0], vmin = __int_as_float(sm.ri[0]);
 #pragma unroll 1
   for (int w = 1; w < SMP_WARPS; ++w) {
-    m = fmaxf(m, s_rf[w]);
-    vmin = fminf(vmin, __int_as_float(s_ri[w]));
+    m = fmaxf(m, sm.rf[w]);
+    vmin = fminf(vmin, __int_as_float(sm.ri[w]));
   }
 
-  // 2. tau = the k'-th largest s, k' = min(top_k, V): the minimum when top_k >= V, else a
-  //    radix select, 8 bits at a time from the top
-  float tau = (a.top_k > 0) ? vmin : -INFINITY;
-  if (a.top_k > 0 && a.top_k < V) {
-    if (tid == 0) {
-      s_prefix = 0u;
-      s_remaining = static_cast<unsigned int>(a.top_k);
-    }
-    unsigned int pmask = 0u;
-#pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) s_hist[tid] = 0u;
-      __syncthreads();
-      const unsigned int prefix = s_prefix;
-      for (int i = tid; i < V; i += SMP_THREADS) {
-        const unsigned int k = fkey(s_s[i]);
-        const bool cand = (k & pmask) == prefix;
-        const unsigned int dig = (k >> shift) & 255u;
-        // aggregate equal digits within the warp: one shared-memory atomic per distinct digit
-        const unsigned int act = __ballot_sync(__activemask(), cand);
-        if (cand) {
-          const unsigned int peers = __match_any_sync(act, dig);
-          if ((__ffs(peers) - 1) == lane) atomicAdd(&s_hist[dig], static_cast<unsigned int>(__popc(peers)));
+  auto val_row = [&](int i) { return s_s[i]; };
+  auto idx_row = [&](int i) { return i; };
+  const unsigned int kk = (a.top_k > 0) ? static_cast<unsigned int>(min(a.top_k, V)) : static_cast<unsigned int>(V);
+  float tau = -INFINITY;
+  if (a.top_k > 0 && kk >= static_cast<unsigned int>(V)) tau = vmin;  // k' = V keeps every entry
+  bool done = false;
+  if (a.top_k > 0 && kk < static_cast<unsigned int>(V)) {
+    bool fast = kk <= static_cast<unsigned int>(SMP_THREADS) && a.cand_cap >= SMP_THREADS;
+    if (fast) {
+      // 2. L = the k'-th largest group maximum (groups past the row's end hold -inf)
+      s_cand[tid] = static_cast<int>(fkey(gmax));
+      const float L = fkey_inv(block_select_desc(
+          [&](int i) { return static_cast<unsigned int>(s_cand[i]); }, SMP_THREADS, kk, sm));
+      // 3. candidates {i : s_i >= L}, compacted in ascending index order; thread t scans a
+      //    contiguous run whose length is a multiple of 4 (16-byte shared-memory loads)
+      const int chunk = ((V + SMP_THREADS - 1) / SMP_THREADS + 3) & ~3;
+      const int i0 = min(V, tid * chunk), i1 = min(V, i0 + chunk);
+      unsigned int cnt = 0;
+      for (int i = i0; i < i1; i += 4) {
+        if (i + 4 <= i1) {
+          const float4 v = *reinterpret_cast<const float4*>(s_s + i);
+          cnt += (v.x >= L) + (v.y >= L) + (v.z >= L) + (v.w >= L);
+        } else {
+          for (int j = i; j < i1; ++j) cnt += s_s[j] >= L;
         }
       }
-      __syncthreads();
-      if (warp == 0) {
-        // lane l owns bins 255-8l .. 248-8l (descending); find the bin holding the remaining-th
-        unsigned int c[8], tot = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          c[j] = s_hist[255 - 8 * lane - j];
-          tot += c[j];
-        }
-        unsigned int incl = tot;  // inclusive prefix over lanes 0..lane (descending bins)
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const unsigned int rem = s_remaining;
-        const unsigned int excl = incl - tot;
-        if (excl < rem && rem <= incl) {
-          unsigned int run = excl;
-          for (int j = 0; j < 8; ++j) {
-            if (run + c[j] >= rem) {
-              const unsigned int dig = 255u - 8u * lane - j;
-              s_remaining = rem - run;
-              s_prefix = prefix | (dig << shift);
-              break;
-            }
-            run += c[j];
+      unsigned long long total = 0;
+      const unsigned long long off = block_scan_u64(cnt, &total, sm);
+      if (total <= static_cast<unsigned long long>(a.cand_cap)) {
+        int o = static_cast<int>(off);
+        for (int i = i0; i < i1; i += 4) {
+          if (i + 4 <= i1) {
+            const float4 v = *reinterpret_cast<const float4*>(s_s + i);
+            if (v.x >= L) s_cand[o++] = i;
+            if (v.y >= L) s_cand[o++] = i + 1;
+            if (v.z >= L) s_cand[o++] = i + 2;
+            if (v.w >= L) s_cand[o++] = i + 3;
+          } else {
+            for (int j = i; j < i1; ++j)
+              if (s_s[j] >= L) s_cand[o++] = j;
           }
         }
+        __syncthreads();
+        const int n = static_cast<int>(total);
+        auto val_c = [&](int j) { return s_s[s_cand[j]]; };
+        auto idx_c = [&](int j) { return s_cand[j]; };
+        // 4. tau among the candidates, then the draw over them
+        tau = fkey_inv(block_select_desc([&](int j) { return fkey(val_c(j)); }, n, kk, sm));
+        draw_over(n, idx_c, val_c, tau, m, a.seed, b, step, emit, sm);
+        done = true;
       }
-      pmask |= 255u << shift;
-      __syncthreads();
     }
-    tau = fkey_inv(s_prefix);
+    if (!done) tau = fkey_inv(block_select_desc([&](int i) { return fkey(s_s[i]); }, V, kk, sm));
   }
-
-  // 3. integer weights over a contiguous chunk per thread, and the block's exclusive scan
-  const int chunk = (V + SMP_THREADS - 1) / SMP_THREADS;
-  const int i0 = tid * chunk, i1 = min(V, i0 + chunk);
-  unsigned long long local = 0;
-  for (int i = i0; i < i1; ++i) {
-    const float s = s_s[i];
-    const unsigned long long w = (s >= tau) ? weight40(s, m) : 0ull;
-    if (a.w_out) a.w_out[static_cast<size_t>(b) * V + i] = w;
-    local += w;
-  }
-  unsigned long long incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) s_ru[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long wt = s_ru[lane];
-    unsigned long long wi = wt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
-    }
-    s_ru[lane] = wi - wt;  // exclusive offset of each warp
-    if (lane == 31) {
-      const unsigned long long W = wi;
-      const unsigned long long r = philox_word0(a.seed, static_cast<unsigned long long>(b),
-                                                static_cast<unsigned long long>(step));
-      s_target = __umul64hi(r, W);
-    }
-  }
-  __syncthreads();
-  const unsigned long long excl = s_ru[warp] + incl - local;
-  const unsigned long long target = s_target;
-  // 4. the thread whose range holds the target walks its chunk
-  if (local > 0 && excl <= target && target < excl + local) {
-    unsigned long long run = excl;
-    for (int i = i0; i < i1; ++i) {
+  if (!done) draw_over(V, idx_row, val_row, tau, m, a.seed, b, step, emit, sm);
+  if (a.w_out) {
+    for (int i = tid; i < V; i += SMP_THREADS) {
       const float s = s_s[i];
-      run += (s >= tau) ? weight40(s, m) : 0ull;
-      if (run > target) {
-        emit(i, tau);
-        break;
-      }
+      a.w_out[static_cast<size_t>(b) * V + i] = (s >= tau) ? weight40(s, m) : 0ull;
     }
   }
 }

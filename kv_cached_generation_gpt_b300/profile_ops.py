@@ -4,6 +4,7 @@
     python -m kv_cached_generation_gpt_b300.profile_ops gemm --m 32768 --n 2304 --k 768 [--block-n 256]
     python -m kv_cached_generation_gpt_b300.profile_ops attn_prefill [--batch 64] [--t 512]
     python -m kv_cached_generation_gpt_b300.profile_ops sample [--batch 64] [--top-k 50]
+    python -m kv_cached_generation_gpt_b300.profile_ops linear_decode --m 64 --n 2304 --k 768 [--gemm-splits 4]
 
 Shapes default to GPT-2 124M (12 heads of 64, vocab 50304, block 1024).  Inputs are seeded
 random tensors; every launch goes through the C ABI and the op status is checked at the end.
@@ -19,7 +20,7 @@ from kv_cached_generation_gpt_b300 import gpt as G
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["attn_decode", "attn_prefill", "gemm", "sample"])
+    ap.add_argument("op", choices=["attn_decode", "attn_prefill", "gemm", "linear_decode", "sample"])
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--heads", type=int, default=12)
     ap.add_argument("--block", type=int, default=1024)
@@ -58,6 +59,11 @@ def main() -> None:
         W = (0.02 * torch.randn(a.n, a.k, device=dev)).to(torch.bfloat16)
         out = torch.empty(a.m, a.n, device=dev)
         run = lambda: G.gpt_linear_bf16(A, W, None, out, a.m, hilo=a.hilo, block_n=a.block_n, splits=a.gemm_splits)
+    elif a.op == "linear_decode":
+        A = torch.randn(2 * a.m, a.k, device=dev).to(torch.bfloat16)
+        W = (0.02 * torch.randn(a.n, a.k, device=dev)).to(torch.bfloat16)
+        out = torch.empty(a.m, a.n, device=dev)
+        run = lambda: G.gpt_linear_decode_bf16(A, W, None, out, a.m, splits=a.gemm_splits)
     else:
         logits = torch.randn(B, a.vocab, device=dev)
         tok = torch.empty(B, dtype=torch.int32, device=dev)

@@ -84,6 +84,70 @@ def test_linear_split_k_is_deterministic():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+# ------------------------------------------------------------------ decode-step Linear (swap-AB, cluster split-K)
+
+
+def _decode_linear_case(M, N, K, splits, seed, with_bias=True):
+    r = _rng(seed)
+    a = r.standard_normal((M, K)).astype(np.float32)
+    w = (r.standard_normal((N, K)) * 0.05).astype(np.float32)
+    b = (r.standard_normal(N) * 0.1).astype(np.float32)
+    A_hi = _bf16(a)
+    A_lo = _bf16(a - A_hi.float().numpy())
+    A = torch.cat([A_hi, A_lo]).cuda()
+    W = _bf16(w).cuda()
+    bias = torch.from_numpy(b).cuda() if with_bias else None
+    out = torch.full((M, N), float("nan"), device="cuda")
+    try:
+        G.gpt_linear_decode_bf16(A, W, bias, out, M, splits=splits)
+    except G.GptError as ex:
+        if ex.code == G.GPT_EUNSUPPORTED and splits == 16:
+            pytest.skip("16-CTA clusters cannot be scheduled on this device")
+        raise
+    _ok()
+    a_eff = _f64(A_hi) + _f64(A_lo)
+    ref = og.linear(a_eff, _f64(W), b.astype(np.float64) if with_bias else None)
+    return out, a, a_eff, W, b, ref
+
+
+@pytest.mark.parametrize("M,N,K,splits", [
+    (1, 64, 64, 1),
+    (1, 2304, 768, 0),         # GPT-2 124M c_attn at B = 1, library-chosen split
+    (3, 200, 128, 2),          # ragged feature tile
+    (8, 768, 768, 8),
+    (17, 3072, 768, 4),        # token rows not a multiple of 8
+    (64, 768, 3072, 16),       # mlp c_proj at B = 64, 16-CTA clusters
+    (64, 2304, 768, 8),
+    (100, 1000, 1024, 2),
+    (128, 768, 768, 8),        # the largest row count
+    (64, 50304, 768, 1),       # lm_head at B = 64
+    (2, 50257, 1024, 0),       # ragged vocabulary, odd row stride of the logits
+    (5, 65, 384, 0),           # 65-symbol vocabulary
+])
+def test_linear_decode_matches_definition(M, N, K, splits):
+    out, a, a_eff, W, b, ref = _decode_linear_case(M, N, K, splits, seed=M * 13 + N + K + splits)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    tol = 2e-6 * math.sqrt(K) * np.max(np.abs(a_eff)) * np.max(np.abs(_f64(W))) * 4 + 1e-6
+    assert np.max(np.abs(got - ref)) < tol
+    # the hi/lo pair carries the fp32 operand to ~16 significant bits
+    assert np.max(np.abs(got - og.linear(a.astype(np.float64), _f64(W), b))) < 50 * tol
+
+
+def test_linear_decode_without_bias_and_deterministic():
+    outs = [_decode_linear_case(64, 768, 3072, 8, seed=5, with_bias=False)[0].cpu() for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_linear_decode_rejects_bad_arguments():
+    A = torch.zeros(2 * 129, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(129, 64, device="cuda")
+    for M, splits in ((129, 1), (0, 1), (4, 3), (4, 2)):  # too many rows, no rows, not a power of 2, > K/64
+        with pytest.raises(G.GptError):
+            G.gpt_linear_decode_bf16(A, W, None, out, M, splits=splits)
+
+
 # ------------------------------------------------------------------ LayerNorm
 
 
@@ -217,6 +281,27 @@ def test_sampler_bit_exact_with_oracle(B, V, T, k):
             assert np.array_equal(w[b], w_ref), (b, np.flatnonzero(w[b] != w_ref)[:5])
             assert thr[b] == osm.topk_threshold(s, k)
             assert tok[b] == osm.sample_row(logits[b], T, k, seed, b, step)
+
+
+@pytest.mark.parametrize("k", [50, 1024, 1025])
+def test_sampler_heavy_ties_match_oracle(k):
+    # Rows whose candidate set above the group-maximum bound is larger than the kernel's
+    # candidate slots (6000 and 50304 tied entries) take the whole-row selection; the 700-way
+    # tie and the plain row take the candidate path (1025 > 1024 groups always the whole row).
+    V = 50304
+    r = _rng(11 + k)
+    logits = (r.standard_normal((4, V)) - 5).astype(np.float32)
+    logits[0, r.choice(V, 6000, replace=False)] = 3.0
+    logits[1, :] = 1.0
+    logits[2, r.choice(V, 700, replace=False)] = 2.5
+    for step in range(3):
+        tok, thr, w = _run_sampler(logits, 0.9, k, 3, step)
+        for b in range(4):
+            s = osm.scaled_logits(logits[b], 0.9)
+            keep = osm.survivors(s, k)
+            assert np.array_equal(w[b], osm.integer_weights(s, keep))
+            assert thr[b] == osm.topk_threshold(s, k)
+            assert tok[b] == osm.sample_row(logits[b], 0.9, k, 3, b, step)
 
 
 def test_sampler_ties_at_threshold_and_greedy():
