@@ -163,7 +163,10 @@ const char* gpt_last_error_detail(void);
  * A (dev, bf16): M x K row-major, or with hilo=1 2M x K (rows [0,M) = hi, [M,2M) = lo parts
  * of one operand, both multiplied into the same fp32 accumulator).  W (dev, bf16): N x K
  * (nn.Linear layout).  bias (dev, fp32, N) or NULL.  K % 64 == 0, 1 <= M, N.
- * block_n: output tile width 64, 128 or 256 (0 = chosen by the library; 256 not with hilo).
+ * block_n: output tile width 64, 128 or 256 (256 not with hilo), or 0 = chosen by the library:
+ * without hilo or split-K, and with at least one 128-row x 256 (N % 256 == 0) or x 128
+ * (N % 128 == 0) tile per SM, the persistent kernel (one CTA per SM walking the tiles, two TMEM
+ * accumulators so the epilogue of one tile overlaps the next tile's MMAs).
  * splits: split-K count >= 1 (needs N % 16 == 0 when > 1); partial sums go to library-owned
  * scratch and are added in split order, so results do not depend on CTA timing. */
 int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,

@@ -280,6 +280,209 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ persistent tcgen05 kernel
+
+// Persistent form for large M (prefill): one CTA per SM walks the output tiles
+// t = blockIdx.x, blockIdx.x + gridDim.x, ... (row-block major, so the CTAs in flight share
+// A row blocks in L2).  Two TMEM accumulators of BN columns: the MMA warp fills one while
+// the epilogue warps drain the other, so the epilogue's global traffic overlaps the next
+// tile's mainloop.  The shared-memory ring's phase runs on across tiles.
+// No split-K, no hi/lo operand.
+template <int BN, int STAGES>
+struct TcPersistSmem {
+  static constexpr uint32_t B_BYTES = BN * TC_BK * 2;
+  static constexpr uint32_t STAGE_BYTES = TC_A_BYTES + B_BYTES;
+  static constexpr uint32_t TILES_BYTES = STAGES * STAGE_BYTES;
+  static constexpr uint32_t STAGE_OFFSET = TILES_BYTES + 256;  // after the ring and the barriers
+  static constexpr uint32_t TOTAL = 1024 + STAGE_OFFSET + 8 * 32 * 20 * 4;  // + a 32 x 20-float buffer per epilogue warp
+};
+
+// The fp32 residual add of one warp's 32 accumulator rows (row0 .. row0+31) over the ncols
+// (multiple of 32) columns starting at n0, TMEM column t_warp.  Thread = row in TMEM, so each
+// 16-column chunk is restaged through this warp's 32 x 20-float shared buffer: afterwards lane
+// l handles rows l/4 + 8i and columns 4*(l%4) .. +3, and the read-modify-write of x goes out
+// in 64-byte runs per row.  The residual of the next 32-column group is in flight while this
+// group is added.
+constexpr int RESID_STAGE_FLOATS = 32 * 20;
+constexpr int PERSIST_THREADS = 320;  // warps 0-7 epilogue (two per TMEM lane quadrant), 8 TMA, 9 MMA
+
+__device__ __forceinline__ void persist_resid_warp(const Epi<__nv_bfloat16>& e, int row0, int n0, int ncols,
+                                                   uint32_t t_warp, float* stage) {
+  const int lane = threadIdx.x & 31;
+  const int sr = lane >> 2, sc = (lane & 3) * 4;
+  const int G = ncols / 32;
+  float4 cur[8], nxt[8];
+  auto load = [&](float4 (&dst)[8], int g) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = row0 + sr + 8 * i, c = n0 + g * 32 + q * 16 + sc;
+        dst[q * 4 + i] = (r < e.M && c < e.N) ? *reinterpret_cast<const float4*>(e.x + static_cast<size_t>(r) * e.ldx + c)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+  };
+  load(cur, 0);
+#pragma unroll 1
+  for (int g = 0; g < G; ++g) {
+    if (g + 1 < G) load(nxt, g + 1);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float v[16];
+      tmem_ld16(t_warp + g * 32 + q * 16, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        reinterpret_cast<float4*>(stage + lane * 20)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = row0 + sr + 8 * i, c = n0 + g * 32 + q * 16 + sc;
+        if (r < e.M && c < e.N) {
+          const float4 a = *reinterpret_cast<const float4*>(stage + (sr + 8 * i) * 20 + sc);
+          const float4 b = e.bias ? *reinterpret_cast<const float4*>(e.bias + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 o = cur[q * 4 + i];
+          *reinterpret_cast<float4*>(e.x + static_cast<size_t>(r) * e.ldx + c) =
+              make_float4(a.x + b.x + o.x, a.y + b.y + o.y, a.z + b.z + o.z, a.w + b.w + o.w);
+        }
+      }
+      __syncwarp();
+    }
+    if (g + 1 < G) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+    }
+  }
+}
+
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(PERSIST_THREADS, 1)
+    gemm_tc_persistent(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int kb_total,
+                       Epi<__nv_bfloat16> e) {
+  using S = TcPersistSmem<BN, STAGES>;
+  static_assert(2 * BN <= 512, "two accumulators must fit in TMEM");
+  constexpr uint32_t TCOLS = 2 * BN <= 256 ? 256 : 512;  // allocation: a power of two
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::TILES_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tm_full = empty + STAGES;   // [2] MMA -> epilogue
+  uint64_t* tm_empty = tm_full + 2;     // [2] epilogue -> MMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tm_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles_n = (e.N + BN - 1) / BN;
+  const int n_tiles = ((e.M + TC_BM - 1) / TC_BM) * n_tiles_n;
+
+  auto a_tile = [&](int s) { return smem + s * S::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return smem + s * S::STAGE_BYTES + TC_A_BYTES; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tm_full[b], 1);
+      mbar_init(&tm_empty[b], 256);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // A comes from the previous kernel
+
+  if (warp == 8) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        const int m_blk = t / n_tiles_n, n_blk = t - m_blk * n_tiles_n;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, e.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
+          tma_load_2d(&tmA, &full[s], a_tile(s), kb * TC_BK, m_blk * TC_BM);
+          tma_load_2d(&tmB, &full[s], b_tile(s), kb * TC_BK, n_blk * BN);
+        }
+      }
+      // Drain: the most recent load into each stage has landed before shared memory is released.
+      for (int i = max(0, it - STAGES); i < it; ++i) mbar_wait(&full[i % STAGES], (i / STAGES) & 1, e.err);
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+      int it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++lt) {
+        const int buf = lt & 1, use = lt >> 1;
+        if (use > 0 && !mbar_wait(&tm_empty[buf], (use & 1) ^ 1, e.err)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, e.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(a_tile(s)), b0 = smem_u32(b_tile(s));
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k)
+            umma_bf16(acc, sdesc_sw128(a0 + 32 * k), sdesc_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&tm_full[buf]);
+      }
+    }
+  } else {
+    // Epilogue warps 0..7: warp w owns TMEM lanes 32(w%4) .. +31 (accumulator rows) and
+    // columns [(w/4) BN/2, (w/4 + 1) BN/2) of the tile.
+    const int quad = warp & 3, half = warp >> 2;
+    constexpr int HALF = BN / 2;
+    int lt = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
+      const int m_blk = t / n_tiles_n, n_blk = t - m_blk * n_tiles_n;
+      const int buf = lt & 1, use = lt >> 1;
+      const bool ok = mbar_wait(&tm_full[buf], use & 1, e.err);
+      tc_fence_after();
+      const int row = m_blk * TC_BM + quad * 32 + lane;
+      const uint32_t t_row =
+          tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN + half * HALF);
+      if (EPI == EPI_RESID && ok) {
+        persist_resid_warp(e, m_blk * TC_BM + quad * 32, n_blk * BN + half * HALF, HALF, t_row,
+                           reinterpret_cast<float*>(smem + S::STAGE_OFFSET) + warp * RESID_STAGE_FLOATS);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < HALF; c += 16) {
+          float v[16];
+          tmem_ld16(t_row + c, v);
+          if (ok) epi_apply16<EPI>(e, row, n_blk * BN + half * HALF + c, v);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tm_empty[buf]);
+      if (!ok) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TCOLS);
+  }
+}
+
 // ------------------------------------------------------------------ fp32 kernel
 
 // 64x64 output tile, 256 threads, 4x4 outputs per thread, K in steps of 16.

@@ -151,6 +151,99 @@ cudaError_t dispatch_tc(int bn, bool hilo, int epi, int dev, const CUtensorMap& 
   return cudaErrorInvalidValue;
 }
 
+// Persistent prefill GEMMs: BN 256 with 4 stages or BN 128 with 6 (192 KiB of ring either way).
+template <int BN>
+constexpr int persist_stages() {
+  return BN == 256 ? 4 : BN == 192 ? 5 : 6;
+}
+
+// Tile width of a persistent GEMM: among 256, 192 and 128 (dividing N), the one whose tile
+// count fills the last wave of num_sms CTAs best (ties: the wider tile); 0 if none applies
+// or there are fewer tiles than SMs.
+int persist_bn(int M, int N, int num_sms) {
+  int best = 0;
+  double best_eff = 0.0;
+  for (int bn : {256, 192, 128}) {
+    if (N % bn != 0) continue;
+    const long long tiles = static_cast<long long>(cdiv(M, TC_BM)) * (N / bn);
+    if (tiles < num_sms) continue;
+    const double eff = static_cast<double>(tiles) / (static_cast<double>(cdiv(tiles, num_sms)) * num_sms);
+    if (eff > best_eff + 1e-3) {
+      best = bn;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
+template <int BN, int EPI>
+cudaError_t attr_persist() {
+  using S = TcPersistSmem<BN, persist_stages<BN>()>;
+  return cudaFuncSetAttribute(gemm_tc_persistent<BN, persist_stages<BN>(), EPI>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::TOTAL);
+}
+
+cudaError_t init_persist_attrs_once();
+
+cudaError_t init_persist_attrs() {
+  cudaError_t r;
+  if ((r = attr_persist<256, EPI_F32>()) != cudaSuccess) return r;
+  if ((r = attr_persist<256, EPI_RESID>()) != cudaSuccess) return r;
+  if ((r = attr_persist<256, EPI_GELU>()) != cudaSuccess) return r;
+  if ((r = attr_persist<256, EPI_QKV>()) != cudaSuccess) return r;
+  if ((r = attr_persist<192, EPI_F32>()) != cudaSuccess) return r;
+  if ((r = attr_persist<192, EPI_RESID>()) != cudaSuccess) return r;
+  if ((r = attr_persist<192, EPI_GELU>()) != cudaSuccess) return r;
+  if ((r = attr_persist<192, EPI_QKV>()) != cudaSuccess) return r;
+  if ((r = attr_persist<128, EPI_F32>()) != cudaSuccess) return r;
+  if ((r = attr_persist<128, EPI_RESID>()) != cudaSuccess) return r;
+  if ((r = attr_persist<128, EPI_GELU>()) != cudaSuccess) return r;
+  return attr_persist<128, EPI_QKV>();
+}
+
+// Once per device (the stand-alone operations have no gpt_create to do it).
+cudaError_t init_persist_attrs_once() {
+  static unsigned long long mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t r = cudaGetDevice(&dev);
+  if (r != cudaSuccess) return r;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 64 && (mask & (1ull << dev))) return cudaSuccess;
+  if ((r = init_persist_attrs()) != cudaSuccess) return r;
+  if (dev < 64) mask |= 1ull << dev;
+  return cudaSuccess;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_persist_epi(const CUtensorMap& ta, const CUtensorMap& tb, int K, int grid, const Epi<bf16>& e,
+                               cudaStream_t st) {
+  constexpr int STAGES = persist_stages<BN>();
+  using S = TcPersistSmem<BN, STAGES>;
+  gemm_tc_persistent<BN, STAGES, EPI><<<grid, PERSIST_THREADS, S::TOTAL, st>>>(ta, tb, K / TC_BK, e);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_persist(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, int K, int grid,
+                           const Epi<bf16>& e, cudaStream_t st) {
+#define KVGPT_PERSIST_CASE(BN, E) \
+  if (bn == BN && epi == E) return launch_persist_epi<BN, E>(ta, tb, K, grid, e, st);
+  KVGPT_PERSIST_CASE(256, EPI_F32)
+  KVGPT_PERSIST_CASE(256, EPI_RESID)
+  KVGPT_PERSIST_CASE(256, EPI_GELU)
+  KVGPT_PERSIST_CASE(256, EPI_QKV)
+  KVGPT_PERSIST_CASE(192, EPI_F32)
+  KVGPT_PERSIST_CASE(192, EPI_RESID)
+  KVGPT_PERSIST_CASE(192, EPI_GELU)
+  KVGPT_PERSIST_CASE(192, EPI_QKV)
+  KVGPT_PERSIST_CASE(128, EPI_F32)
+  KVGPT_PERSIST_CASE(128, EPI_RESID)
+  KVGPT_PERSIST_CASE(128, EPI_GELU)
+  KVGPT_PERSIST_CASE(128, EPI_QKV)
+#undef KVGPT_PERSIST_CASE
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t set_tc_attr(int bn, bool hilo, int epi, int dev) {
 #define KVGPT_TC_ATTR(BN, H, E, SLOT) \
   if (bn == BN && hilo == H && epi == E) return attr_tc<BN, H, E>(SLOT, dev);
@@ -321,6 +414,8 @@ cudaError_t init_kernel_attrs(int dev) {
         cudaError_t r = set_tc_attr(bns[bi], h != 0, epi, dev);
         if (r != cudaSuccess) return r;
       }
+  cudaError_t r = init_persist_attrs();
+  if (r != cudaSuccess) return r;
   return init_dl_attrs(dev);
 }
 
@@ -361,6 +456,19 @@ __global__ void advance_kernel(int* pos, int* step) {
   griddep_wait();
   *pos += 1;
   *step += 1;
+}
+
+// LayerNorm launch with the register bound matched to C (pairs per lane = C / 64).
+template <typename TO>
+cudaError_t launch_ln(int rows, int C, long long in_stride, const float* x, const float* gamma, const float* beta,
+                      TO* y, TO* y_lo, int ldy, cudaStream_t st, bool pdl) {
+  const dim3 grid(cdiv(rows, 8)), block(256);
+  if (C <= 12 * 64)
+    return launch_k(layernorm_kernel<TO, 12>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta, y, y_lo, ldy);
+  if (C <= 16 * 64)
+    return launch_k(layernorm_kernel<TO, 16>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta, y, y_lo, ldy);
+  return launch_k(layernorm_kernel<TO, LN_MAX_PAIRS>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta, y,
+                  y_lo, ldy);
 }
 
 int map_error_word(int w) {
@@ -543,6 +651,22 @@ void free_model(gpt_model* m) {
 // y = A W^T with the given epilogue, bf16 operands.  A has M rows (2M with hilo).
 int gemm_bf16(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, bool hilo, int epi, Epi<bf16> e,
               bool allow_split) {
+  // Enough 128 x BN tiles for every SM: the persistent kernel (one CTA per SM).
+  const int bnp = hilo ? 0 : persist_bn(M, N, m->num_sms);
+  if (bnp) {
+    CUtensorMap ta, tb;
+    int rc = make_tmap(&ta, A, M, K, TC_BM);
+    if (rc) return rc;
+    rc = m->weight_map(W, N, K, bnp, &tb);
+    if (rc) return rc;
+    e.M = M;
+    e.N = N;
+    e.splits = 1;
+    e.err = m->d_err;
+    CK(launch_persist(bnp, epi, ta, tb, K, m->num_sms, e, m->stream));
+    ++m->launches;
+    return GPT_OK;
+  }
   GemmPlan p = plan_gemm(M, N, K, m->num_sms, hilo, m->ws_bytes);
   if (!allow_split) p.splits = 1;
   if (p.splits > 1 && static_cast<size_t>(cdiv(M, TC_BM)) * cdiv(N, p.bn) > m->n_tickets) p.splits = 1;
@@ -632,9 +756,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     TE* kc = static_cast<TE*>(m->kcache(l));
     TE* vc = static_cast<TE*>(m->vcache(l));
     // ln_1
-    CK(launch_k(layernorm_kernel<TE>, dim3(cdiv(rows, rows_per_cta)), dim3(256), 0, st, pdl, m->x, rows, C,
-                static_cast<long long>(C), w.ln1_w, w.ln1_b, xn,
-                hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C));
+    CK(launch_ln<TE>(rows, C, C, m->x, w.ln1_w, w.ln1_b, xn,
+                     hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
     ++m->launches;
     // c_attn + KV append
     {
@@ -695,9 +818,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       if (rc) return rc;
     }
     // ln_2
-    CK(launch_k(layernorm_kernel<TE>, dim3(cdiv(rows, rows_per_cta)), dim3(256), 0, st, pdl, m->x, rows, C,
-                static_cast<long long>(C), w.ln2_w, w.ln2_b, xn,
-                hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C));
+    CK(launch_ln<TE>(rows, C, C, m->x, w.ln2_w, w.ln2_b, xn,
+                     hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
     ++m->launches;
     // mlp c_fc + GELU
     {
@@ -730,10 +852,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     }
   }
   // ln_f on the last position of each sequence, then the tied lm_head
-  CK(launch_k(layernorm_kernel<TE>, dim3(cdiv(B, rows_per_cta)), dim3(256), 0, st, pdl,
-              static_cast<const float*>(m->x + static_cast<size_t>(T - 1) * C), B, C, static_cast<long long>(T) * C,
-              static_cast<const float*>(m->ln_f_w), static_cast<const float*>(m->ln_f_b), xf,
-              kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C));
+  CK(launch_ln<TE>(B, C, static_cast<long long>(T) * C, m->x + static_cast<size_t>(T - 1) * C, m->ln_f_w, m->ln_f_b,
+                   xf, kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C, st, pdl));
   ++m->launches;
   {
     Epi<TE> e;
@@ -1086,6 +1206,27 @@ int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out,
   CK(cudaGetDevice(&dev));
   int num_sms = 148;
   CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  if (block_n == 0 && splits == 1 && !hilo) {
+    const int bnp = persist_bn(M, N, num_sms);
+    if (bnp) {
+      OpCtx* c = nullptr;
+      int rc = op_ctx(&c, 0, 0);
+      if (rc) return rc;
+      CK(init_persist_attrs_once());
+      CUtensorMap ta, tb;
+      if ((rc = make_tmap(&ta, A, M, K, TC_BM))) return rc;
+      if ((rc = make_tmap(&tb, W, N, K, bnp))) return rc;
+      Epi<bf16> e;
+      e.M = M;
+      e.N = N;
+      e.bias = bias;
+      e.x = out;
+      e.ldx = N;
+      e.err = c->err;
+      CK(launch_persist(bnp, EPI_F32, ta, tb, K, num_sms, e, static_cast<cudaStream_t>(stream)));
+      return GPT_OK;
+    }
+  }
   GemmPlan p = plan_gemm(M, N, K, num_sms, hilo != 0, ~size_t(0));
   if (block_n) p.bn = block_n;
   p.splits = std::min(splits, K / TC_BK);
@@ -1152,12 +1293,11 @@ int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const fl
   if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == GPT_DTYPE_BF16)
-    layernorm_kernel<bf16><<<cdiv(rows, 8), 256, 0, st>>>(x, rows, C, x_stride, gamma, beta, static_cast<bf16*>(y),
-                                                          static_cast<bf16*>(y_lo), C);
+    CK(launch_ln<bf16>(rows, C, x_stride, x, gamma, beta, static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, st,
+                       false));
   else
-    layernorm_kernel<float><<<cdiv(rows, 8), 256, 0, st>>>(x, rows, C, x_stride, gamma, beta, static_cast<float*>(y),
-                                                           nullptr, C);
-  CK(cudaGetLastError());
+    CK(launch_ln<float>(rows, C, x_stride, x, gamma, beta, static_cast<float*>(y), static_cast<float*>(nullptr), C, st,
+                        false));
   return GPT_OK;
 }
 

@@ -44,9 +44,15 @@ __global__ void embed_kernel(const int* __restrict__ tokens, int rows, int T, co
   }
 }
 
+__device__ __forceinline__ void store_pair(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
+__device__ __forceinline__ void store_pair(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
 // y[r, :] = LN(x[r * in_stride + :]) for r < rows; warp per row.  TO is bf16 or f32.
 // With y_lo, also writes the rounding remainder y - bf16(y) (the lo half of a hi/lo pair).
-template <typename TO>
+// MAXP bounds C / 64 (the float pairs a lane holds), so small models keep few registers.
+template <typename TO, int MAXP = LN_MAX_PAIRS>
 __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, long long in_stride,
                                  const float* __restrict__ gamma, const float* __restrict__ beta,
                                  TO* __restrict__ y, TO* __restrict__ y_lo, int ldy) {
@@ -57,10 +63,10 @@ __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, l
   if (r >= rows) return;
   const float* xr = x + static_cast<size_t>(r) * in_stride;
   const int np = C / 64;
-  float2 v[LN_MAX_PAIRS];
+  float2 v[MAXP];
   float s = 0.0f;
 #pragma unroll
-  for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+  for (int i = 0; i < MAXP; ++i) {
     if (i < np) {
       v[i] = *reinterpret_cast<const float2*>(xr + i * 64 + lane * 2);
       s += v[i].x + v[i].y;
@@ -69,7 +75,7 @@ __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, l
   const float mean = warp_sum(s) / static_cast<float>(C);
   float q = 0.0f;
 #pragma unroll
-  for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+  for (int i = 0; i < MAXP; ++i) {
     if (i < np) {
       const float a = v[i].x - mean, b = v[i].y - mean;
       q += a * a + b * b;
@@ -79,22 +85,21 @@ __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, l
   const float rstd = 1.0f / sqrtf(var + 1e-5f);
   TO* yr = y + static_cast<size_t>(r) * ldy;
 #pragma unroll
-  for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+  for (int i = 0; i < MAXP; ++i) {
     if (i < np) {
       const int c = i * 64 + lane * 2;
-      float a = (v[i].x - mean) * rstd * gamma[c];
-      float b = (v[i].y - mean) * rstd * gamma[c + 1];
+      const float2 g2 = *reinterpret_cast<const float2*>(gamma + c);
+      float a = (v[i].x - mean) * rstd * g2.x;
+      float b = (v[i].y - mean) * rstd * g2.y;
       if (beta) {
-        a += beta[c];
-        b += beta[c + 1];
+        const float2 b2 = *reinterpret_cast<const float2*>(beta + c);
+        a += b2.x;
+        b += b2.y;
       }
-      const TO ha = from_f32<TO>(a), hb = from_f32<TO>(b);
-      yr[c] = ha;
-      yr[c + 1] = hb;
+      store_pair(yr + c, a, b);
       if (y_lo) {
-        TO* lr = y_lo + static_cast<size_t>(r) * ldy;
-        lr[c] = from_f32<TO>(a - to_f32(ha));
-        lr[c + 1] = from_f32<TO>(b - to_f32(hb));
+        const float ha = to_f32(from_f32<TO>(a)), hb = to_f32(from_f32<TO>(b));
+        store_pair(y_lo + static_cast<size_t>(r) * ldy + c, a - ha, b - hb);
       }
     }
   }

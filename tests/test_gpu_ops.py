@@ -43,6 +43,10 @@ def _ok():
     (3, 50304, 768, 128, 1, True),        # lm_head shape, hi/lo
     (2, 50257, 1024, 64, 1, True),        # ragged vocabulary (N % 16 != 0)
     (1000, 1024, 4096, 256, 1, False),    # 350M mlp proj, several tiles each way
+    (4100, 2304, 768, 0, 1, False),       # persistent kernel, 128 x 256 tiles, ragged last row block
+    (4096, 1152, 384, 0, 1, False),       # persistent kernel, 128 x 128 tiles
+    (19000, 768, 3072, 0, 1, False),      # persistent kernel, several tiles per CTA, long K
+    (4736, 3072, 256, 0, 1, False),       # persistent kernel, 128 x 256 tiles (3 full waves)
 ])
 def test_linear_bf16_matches_definition(M, N, K, block_n, splits, hilo):
     r = _rng(M * 7 + N + K)
