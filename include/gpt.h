@@ -137,6 +137,16 @@ int gpt_generate(gpt_model_t* model, const int32_t* idx, int32_t B, int32_t T, i
  * be NULL.  GPT_ESTATE if no gpt_generate ran yet. */
 int gpt_last_timing(gpt_model_t* model, float* prefill_ms, float* decode_ms);
 
+/* GEMM timing of prefills, for profiling.  enable = 1: every later prefill (gpt_prefill, or the
+ * prefill part of gpt_generate) records CUDA events on the model's stream around each of its
+ * Linear-layer launches (the lm_head excluded); 0 stops it.  Decode steps are never timed. */
+int gpt_profile_gemms(gpt_model_t* model, int32_t enable);
+
+/* Summed device time (ms, from the events) and FLOPs (2 M N K each) of the Linear layers of the
+ * last timed prefill.  Synchronises on its last event.  Either pointer may be NULL.
+ * GPT_ESTATE if no prefill was timed. */
+int gpt_gemm_timing(gpt_model_t* model, float* ms, double* flops);
+
 /* Current cache length (host-side mirror), or -1 for NULL. */
 int32_t gpt_cache_length(const gpt_model_t* model);
 

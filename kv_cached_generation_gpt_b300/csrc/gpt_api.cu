@@ -601,6 +601,11 @@ struct gpt_model {
   long long graph_kernels = 0;  // kernel nodes in the captured decode-step graph
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool timing_valid = false;
+  // GEMM timing of prefills (gpt_profile_gemms): events around every prefill GEMM launch
+  bool prof_enabled = false, prof_active = false;
+  std::vector<cudaEvent_t> prof_ev;
+  size_t prof_n = 0;      // events recorded by the last profiled prefill
+  double prof_flops = 0;  // 2 M N K summed over its GEMMs
   std::map<std::tuple<uintptr_t, long long, long long, int>, CUtensorMap> wmaps;
 
   template <typename T>
@@ -643,14 +648,33 @@ void free_model(gpt_model* m) {
   if (m->gexec) cudaGraphExecDestroy(m->gexec);
   for (auto& e : m->ev)
     if (e) cudaEventDestroy(e);
+  for (auto& e : m->prof_ev)
+    if (e) cudaEventDestroy(e);
   for (void* p : m->allocs) cudaFree(p);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   delete m;
 }
 
 // y = A W^T with the given epilogue, bf16 operands.  A has M rows (2M with hilo).
+int gemm_bf16_launch(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, bool hilo, int epi, Epi<bf16> e,
+                     bool allow_split);
+
 int gemm_bf16(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, bool hilo, int epi, Epi<bf16> e,
               bool allow_split) {
+  const bool prof = m->prof_active && m->prof_n + 2 <= m->prof_ev.size();
+  if (prof) CK(cudaEventRecord(m->prof_ev[m->prof_n], m->stream));
+  const int rc = gemm_bf16_launch(m, A, W, M, N, K, hilo, epi, e, allow_split);
+  if (rc) return rc;
+  if (prof) {
+    CK(cudaEventRecord(m->prof_ev[m->prof_n + 1], m->stream));
+    m->prof_n += 2;
+    m->prof_flops += 2.0 * M * N * K;
+  }
+  return GPT_OK;
+}
+
+int gemm_bf16_launch(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, bool hilo, int epi, Epi<bf16> e,
+                     bool allow_split) {
   // Enough 128 x BN tiles for every SM: the persistent kernel (one CTA per SM).
   const int bnp = hilo ? 0 : persist_bn(M, N, m->num_sms);
   if (bnp) {
@@ -871,8 +895,15 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
 }
 
 int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits) {
-  return m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits)
-                 : enqueue_forward<float>(m, tokens, B, T, decode, logits);
+  m->prof_active = m->prof_enabled && !decode;
+  if (m->prof_active) {
+    m->prof_n = 0;
+    m->prof_flops = 0;
+  }
+  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits)
+                         : enqueue_forward<float>(m, tokens, B, T, decode, logits);
+  m->prof_active = false;
+  return rc;
 }
 
 int enqueue_sample(gpt_model* m, int B, float temperature, int top_k, unsigned long long seed, const int* step_dev,
@@ -1181,6 +1212,33 @@ int gpt_last_timing(gpt_model_t* m, float* prefill_ms, float* decode_ms) {
   CK(cudaEventElapsedTime(&b, m->ev[1], m->ev[2]));
   if (prefill_ms) *prefill_ms = a;
   if (decode_ms) *decode_ms = b;
+  return GPT_OK;
+}
+
+int gpt_profile_gemms(gpt_model_t* m, int32_t enable) {
+  if (!m) return GPT_EINVAL;
+  if (enable && m->prof_ev.empty()) {
+    m->prof_ev.assign(8 * static_cast<size_t>(std::max(1, m->L)) + 8, nullptr);
+    for (auto& e : m->prof_ev) CK(cudaEventCreate(&e));
+  }
+  m->prof_enabled = enable != 0;
+  m->prof_n = 0;
+  m->prof_flops = 0;
+  return GPT_OK;
+}
+
+int gpt_gemm_timing(gpt_model_t* m, float* ms, double* flops) {
+  if (!m) return GPT_EINVAL;
+  if (m->prof_n == 0) return GPT_ESTATE;
+  CK(cudaEventSynchronize(m->prof_ev[m->prof_n - 1]));
+  float total = 0.0f;
+  for (size_t i = 0; i + 1 < m->prof_n; i += 2) {
+    float t = 0.0f;
+    CK(cudaEventElapsedTime(&t, m->prof_ev[i], m->prof_ev[i + 1]));
+    total += t;
+  }
+  if (ms) *ms = total;
+  if (flops) *flops = m->prof_flops;
   return GPT_OK;
 }
 

@@ -33,7 +33,7 @@ EXPORTED = (
     "gpt_create", "gpt_destroy", "gpt_prefill", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
     "gpt_cache_length", "gpt_kernel_launches", "gpt_sync_status", "gpt_strerror", "gpt_last_error_detail", "gpt_linear_bf16",
     "gpt_layernorm", "gpt_attention_prefill", "gpt_attention_decode", "gpt_sample", "gpt_op_status",
-    "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16",
+    "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16", "gpt_profile_gemms", "gpt_gemm_timing",
 )
 
 c_int32, c_void_p, c_float, c_uint64, c_int64 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float, ctypes.c_uint64, ctypes.c_int64
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
                                             c_uint64, c_void_p]),
             "gpt_last_timing": (ctypes.c_int, [c_void_p, P(c_float), P(c_float)]),
             "gpt_cache_length": (c_int32, [c_void_p]),
+            "gpt_profile_gemms": (ctypes.c_int, [c_void_p, c_int32]),
+            "gpt_gemm_timing": (ctypes.c_int, [c_void_p, P(c_float), P(ctypes.c_double)]),
             "gpt_kernel_launches": (c_int64, [c_void_p]),
             "gpt_sync_status": (ctypes.c_int, [c_void_p]),
             "gpt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -187,6 +189,17 @@ def gpt_last_timing(model: int) -> tuple[float, float]:
     a, b = c_float(), c_float()
     _check(lib().gpt_last_timing(model, ctypes.byref(a), ctypes.byref(b)), "gpt_last_timing")
     return a.value, b.value
+
+
+def gpt_profile_gemms(model: int, enable: bool) -> None:
+    _check(lib().gpt_profile_gemms(model, 1 if enable else 0), "gpt_profile_gemms")
+
+
+def gpt_gemm_timing(model: int) -> tuple[float, float]:
+    """(ms, FLOPs) of the Linear layers of the last timed prefill."""
+    ms, fl = c_float(), ctypes.c_double()
+    _check(lib().gpt_gemm_timing(model, ctypes.byref(ms), ctypes.byref(fl)), "gpt_gemm_timing")
+    return ms.value, fl.value
 
 
 def gpt_cache_length(model: int) -> int:

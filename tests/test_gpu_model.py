@@ -180,3 +180,23 @@ def test_error_paths():
     assert ei.value.code == G.GPT_ECONTEXT
     assert model.sync_status() == G.GPT_OK
     model.close()
+
+
+def test_prefill_gemm_timing_counts_the_linear_layers():
+    """gpt_profile_gemms: events around every prefill Linear layer; FLOPs = sum of 2 M N K."""
+    shape = syn.ModelShape(2, 2, 128, 96, 300, False, "bf16")
+    sd = syn.make_weights(shape, seed=5)
+    model = make_gpu_model(shape, sd, 2)
+    tokens = torch.from_numpy(syn.make_tokens(2, 40, shape.vocab_size, seed=6)).cuda()
+    with pytest.raises(G.GptError):
+        G.gpt_gemm_timing(model.handle)  # nothing timed yet
+    G.gpt_profile_gemms(model.handle, True)
+    model.prefill(tokens)
+    ms, flops = G.gpt_gemm_timing(model.handle)
+    C, L, M = shape.n_embd, shape.n_layer, 2 * 40
+    assert flops == 2.0 * M * 12 * C * C * L  # c_attn 3C^2, c_proj C^2, c_fc and mlp c_proj 4C^2 each
+    assert ms > 0.0
+    model.decode_step(tokens[:, 0].contiguous())  # decode steps are not timed: the prefill's numbers stay
+    assert G.gpt_gemm_timing(model.handle)[1] == flops
+    G.gpt_profile_gemms(model.handle, False)
+    assert model.sync_status() == G.GPT_OK
