@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
 
 // ------------------------------------------------------------------ prefill, bf16 tensor cores
 
-constexpr int PF_BQ = 64, PF_BKEY = 64, PF_THREADS = 128;
+constexpr int PF_BQ = 64, PF_BKEY = 64, PF_THREADS = 128;  // 4 warps x 16 query rows
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -261,11 +261,12 @@ __device__ __forceinline__ void cp_async_wait() {
 // Byte offset of 16-byte chunk c of row r in a 64 x 64 bf16 tile with XOR swizzle.
 __device__ __forceinline__ uint32_t swz(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-// Copy rows [row0, row0+64) of a [rows][64] bf16 matrix into a swizzled tile; rows >= nvalid are zeros.
+// Copy rows [row0, row0+ROWS) of a [rows][64] bf16 matrix into a swizzled tile; rows >= nvalid are zeros.
+template <int ROWS>
 __device__ __forceinline__ void load_tile64(uint32_t tile, const __nv_bfloat16* src, int row0, int nvalid) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + i * PF_THREADS;  // 512 chunks of 16 B
+  for (int i = 0; i < ROWS * 8 / PF_THREADS; ++i) {
+    const int idx = threadIdx.x + i * PF_THREADS;  // ROWS x 8 chunks of 16 B
     const int r = idx >> 3, c = idx & 7;
     const bool ok = row0 + r < nvalid;
     const __nv_bfloat16* p = src + static_cast<size_t>(ok ? row0 + r : 0) * HS + c * 8;
@@ -274,6 +275,7 @@ __device__ __forceinline__ void load_tile64(uint32_t tile, const __nv_bfloat16* 
 }
 
 // grid (ceil(T/64), B*nh).  Queries t in [0, T) sit at positions pos0 + t; keys 0..pos0+T-1.
+// Query blocks run heaviest (most keys) first: block qb = gridDim.x - 1 - blockIdx.x.
 __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloat16* __restrict__ q,
                                                                 const __nv_bfloat16* __restrict__ kc,
                                                                 const __nv_bfloat16* __restrict__ vc, int nh, int T,
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloa
   __shared__ __align__(128) __nv_bfloat16 sQ[PF_BQ * HS];
   __shared__ __align__(128) __nv_bfloat16 sK[2][PF_BKEY * HS];
   __shared__ __align__(128) __nv_bfloat16 sV[2][PF_BKEY * HS];
-  const int qb = blockIdx.x, bh = blockIdx.y;
+  const int qb = gridDim.x - 1 - blockIdx.x, bh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int q0 = qb * PF_BQ;
@@ -295,9 +297,9 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloa
   constexpr uint32_t TILE_BYTES = PF_BKEY * HS * 2;
   const uint32_t sq = smem_u32(sQ), sk0 = smem_u32(sK[0]), sv0 = smem_u32(sV[0]);
 
-  load_tile64(sq, qg, q0, T);
-  load_tile64(sk0, kg, 0, n_keys);
-  load_tile64(sv0, vg, 0, n_keys);
+  load_tile64<PF_BQ>(sq, qg, q0, T);
+  load_tile64<PF_BKEY>(sk0, kg, 0, n_keys);
+  load_tile64<PF_BKEY>(sv0, vg, 0, n_keys);
   cp_async_commit();
 
   uint32_t qa[4][4];  // A fragments of this warp's 16 query rows, 4 k-steps of 16 dims
@@ -314,8 +316,8 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloa
     const int buf = kb & 1;
     const uint32_t skb = sk0 + buf * TILE_BYTES, svb = sv0 + buf * TILE_BYTES;
     if (kb + 1 < n_kb) {
-      load_tile64(sk0 + (buf ^ 1) * TILE_BYTES, kg, (kb + 1) * PF_BKEY, n_keys);
-      load_tile64(sv0 + (buf ^ 1) * TILE_BYTES, vg, (kb + 1) * PF_BKEY, n_keys);
+      load_tile64<PF_BKEY>(sk0 + (buf ^ 1) * TILE_BYTES, kg, (kb + 1) * PF_BKEY, n_keys);
+      load_tile64<PF_BKEY>(sv0 + (buf ^ 1) * TILE_BYTES, vg, (kb + 1) * PF_BKEY, n_keys);
     }
     cp_async_commit();
     cp_async_wait<1>();
