@@ -19,10 +19,16 @@
 //
 // Programmatic dependent launch: weight tiles do not depend on earlier kernels, so they are
 // requested before griddepcontrol.wait; activations, residual and outputs come after it.
+//
+// Up to 8 token rows, the LayerNorm before c_attn, c_fc and the lm_head runs inside this
+// kernel: every CTA reads the whole fp32 rows (a few KiB), takes their statistics exactly as
+// layernorm_kernel does, and writes its K-slice of LN(x) as the bf16 hi/lo operand straight
+// into the swizzled shared-memory tile the MMA reads, so no LayerNorm launch is needed.
 #pragma once
 
 #include "common.cuh"
 #include "gemm.cuh"
+#include "norm.cuh"
 
 namespace kvgpt {
 
@@ -30,6 +36,7 @@ constexpr int DL_THREADS = 192;  // warps 0-3: TMEM -> partial; warp 4: TMA; war
 constexpr int DL_MAX_STAGES = 3;
 constexpr int DL_MAX_ROWS = 128;
 constexpr int DL_MAX_SPLITS = 16;
+constexpr int DL_LN_MAX_ROWS = 8;   // in-kernel LayerNorm operand up to this many token rows
 constexpr uint32_t DL_W_BYTES = 128u * TC_BK * 2u;
 
 __host__ __device__ constexpr int dl_bp(int rows) { return (rows + 7) & ~7; }
@@ -142,7 +149,10 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
   uint64_t* empty = full + DL_MAX_STAGES;
   uint64_t* acc_full = empty + DL_MAX_STAGES;
   uint64_t* recv_full = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_full + 1);
+  uint64_t* x_full = recv_full + 1;  // [DL_MAX_STAGES]: operand written by warps 0-3 (LayerNorm)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + DL_MAX_STAGES);
+  const bool lnx = e.ln_x != nullptr;
+  __shared__ float s_mean[DL_LN_MAX_ROWS], s_rstd[DL_LN_MAX_ROWS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -167,6 +177,7 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
     }
     mbar_init(acc_full, 1);
     mbar_init(recv_full, 1);
+    for (int s = 0; s < stages; ++s) mbar_init(&x_full[s], 128);
     fence_mbar_init();
     // the S - 1 peers' slices for this CTA complete on recv_full
     if (splits > 1) mbar_arrive_expect_tx(recv_full, static_cast<uint32_t>(splits - 1) * slice_bytes);
@@ -186,24 +197,29 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmX);
       const int pre = min(nkb, stages);
+      const uint32_t tx = lnx ? DL_W_BYTES : DL_W_BYTES + x_bytes;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], DL_W_BYTES + x_bytes);
+        mbar_arrive_expect_tx(&full[i], tx);
         tma_load_2d(&tmW, &full[i], w_tile(i), (kb0 + i) * TC_BK, tile * 128);
       }
       griddep_wait();  // activations come from the previous kernel
-      for (int i = 0; i < pre; ++i) {
-        tma_load_2d(&tmX, &full[i], x_tile(i), (kb0 + i) * TC_BK, 0);
-        tma_load_2d(&tmX, &full[i], x_tile(i) + bp * 128, (kb0 + i) * TC_BK, e.M);
+      if (!lnx) {
+        for (int i = 0; i < pre; ++i) {
+          tma_load_2d(&tmX, &full[i], x_tile(i), (kb0 + i) * TC_BK, 0);
+          tma_load_2d(&tmX, &full[i], x_tile(i) + bp * 128, (kb0 + i) * TC_BK, e.M);
+        }
       }
       int issued = pre;
       for (int i = pre; i < nkb; ++i) {
         const int s = i % stages;
         if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, e.err)) break;
-        mbar_arrive_expect_tx(&full[s], DL_W_BYTES + x_bytes);
+        mbar_arrive_expect_tx(&full[s], tx);
         const int kx = (kb0 + i) * TC_BK;
         tma_load_2d(&tmW, &full[s], w_tile(s), kx, tile * 128);
-        tma_load_2d(&tmX, &full[s], x_tile(s), kx, 0);
-        tma_load_2d(&tmX, &full[s], x_tile(s) + bp * 128, kx, e.M);
+        if (!lnx) {
+          tma_load_2d(&tmX, &full[s], x_tile(s), kx, 0);
+          tma_load_2d(&tmX, &full[s], x_tile(s) + bp * 128, kx, e.M);
+        }
         issued = i + 1;
       }
       // Drain: the most recent load into each stage has landed before shared memory is reused.
@@ -215,6 +231,7 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
       for (int i = 0; i < nkb; ++i) {
         const int s = i % stages;
         if (!mbar_wait(&full[s], (i / stages) & 1, e.err)) break;
+        if (lnx && !mbar_wait(&x_full[s], (i / stages) & 1, e.err)) break;
         tc_fence_after();
         const uint32_t a0 = smem_u32(w_tile(s)), b0 = smem_u32(x_tile(s));
 #pragma unroll
@@ -226,6 +243,88 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
       mbar_wait(acc_full, 0, e.err);  // no MMA in flight once this returns
     }
   } else {
+    if (lnx) {
+      // Warps 0-3 first build the operand: LayerNorm statistics of every token row (warp w
+      // takes rows w, w+4: lanes hold column pairs i*64 + 2*lane, as layernorm_kernel does) ...
+      griddep_wait();  // the residual rows come from the previous kernel
+      const int C = kb_total * TC_BK;
+      const int np = C / 64;
+      for (int r = warp; r < e.M; r += 4) {
+        const float* xr = e.ln_x + r * e.ln_ldx;
+        float2 v[LN_MAX_PAIRS];
+#pragma unroll
+        for (int i = 0; i < LN_MAX_PAIRS; ++i)
+          if (i < np) v[i] = *reinterpret_cast<const float2*>(xr + i * 64 + lane * 2);
+        float sm = 0.0f;
+#pragma unroll
+        for (int i = 0; i < LN_MAX_PAIRS; ++i)
+          if (i < np) sm += v[i].x + v[i].y;
+        const float mean = warp_sum(sm) / static_cast<float>(C);
+        float q = 0.0f;
+#pragma unroll
+        for (int i = 0; i < LN_MAX_PAIRS; ++i) {
+          if (i < np) {
+            const float a = v[i].x - mean, b = v[i].y - mean;
+            q += a * a + b * b;
+          }
+        }
+        const float var = warp_sum(q) / static_cast<float>(C);
+        if (lane == 0) {
+          s_mean[r] = mean;
+          s_rstd[r] = 1.0f / sqrtf(var + 1e-5f);
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      // ... then, per k-block, its 64 columns of LN(x) as hi (rows 0..bp-1) and lo (rows
+      // bp..2bp-1) in the 128-byte-swizzled layout a TMA load would have written.
+      const int tid = threadIdx.x;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % stages;
+        if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, e.err)) break;
+        const uint32_t xt = smem_u32(x_tile(s));
+        for (int it = tid; it < bp * 8; it += 128) {
+          const int r = it >> 3, c = it & 7;
+          uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
+          if (r < e.M) {
+            const int k = (kb0 + i) * TC_BK + c * 8;
+            const float4* xp = reinterpret_cast<const float4*>(e.ln_x + r * e.ln_ldx + k);
+            const float4* gp = reinterpret_cast<const float4*>(e.ln_g + k);
+            const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
+            float y[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float mean = s_mean[r], rstd = s_rstd[r];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) y[j] = (y[j] - mean) * rstd * gm[j];
+            if (e.ln_b) {
+              const float4* bp4 = reinterpret_cast<const float4*>(e.ln_b + k);
+              const float4 b0 = bp4[0], b1 = bp4[1];
+              y[0] += b0.x; y[1] += b0.y; y[2] += b0.z; y[3] += b0.w;
+              y[4] += b1.x; y[5] += b1.y; y[6] += b1.z; y[7] += b1.w;
+            }
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * j], y[2 * j + 1]);
+              const float2 hf = __bfloat1622float2(h);
+              hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+              lw[j] = pack_bf16x2(y[2 * j] - hf.x, y[2 * j + 1] - hf.y);
+            }
+            hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+          const uint32_t off_hi = static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+          const uint32_t off_lo = static_cast<uint32_t>((bp + r) * 128 + ((c ^ (r & 7)) << 4));  // bp % 8 == 0
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xt + off_hi), "r"(hi.x), "r"(hi.y), "r"(hi.z),
+                       "r"(hi.w)
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xt + off_lo), "r"(lo.x), "r"(lo.y), "r"(lo.z),
+                       "r"(lo.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();  // the MMA reads the operand through the async proxy
+        mbar_arrive(&x_full[s]);
+      }
+    }
     // Warps 0-3: TMEM lane f = feature f of the tile.  Park hi + lo at park[o][row][f % R] of
     // owner o = f / R, in the ring: every load into it has landed and every MMA reading it
     // has completed.

@@ -53,6 +53,13 @@ struct Epi {
   unsigned int* tickets = nullptr;
   int splits = 1;
   int* err = nullptr;
+  // Decode-step kernel only: the activation operand is LayerNorm(ln_x rows) (ln_g, ln_b
+  // nullable; row r at ln_x + r * ln_ldx, fp32), computed in the kernel, instead of a bf16 hi/lo
+  // operand read by TMA (M <= DL_LN_MAX_ROWS).
+  const float* ln_x = nullptr;
+  long long ln_ldx = 0;
+  const float* ln_g = nullptr;
+  const float* ln_b = nullptr;
 };
 
 // Apply the epilogue to 16 consecutive columns n0..n0+15 of row r (n0 % 16 == 0).

@@ -760,6 +760,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   const bool hilo = kBf16 && decode && m->hilo_decode;
   // decode-shape Linear layers (swap-AB, cluster split-K) and programmatic dependent launches
   const bool dl = hilo && rows <= DL_MAX_ROWS;
+  // up to 8 rows the decode-shape kernels take LayerNorm(x) as their operand directly
+  const bool ln_in = dl && rows <= DL_LN_MAX_ROWS;
   const bool pdl = decode;
   const int* pos0 = decode ? m->d_pos : nullptr;
   cudaStream_t st = m->stream;
@@ -779,10 +781,12 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     const LayerDev& w = m->layers[l];
     TE* kc = static_cast<TE*>(m->kcache(l));
     TE* vc = static_cast<TE*>(m->vcache(l));
-    // ln_1
-    CK(launch_ln<TE>(rows, C, C, m->x, w.ln1_w, w.ln1_b, xn,
-                     hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
-    ++m->launches;
+    // ln_1 (in the c_attn kernel when ln_in)
+    if (!ln_in) {
+      CK(launch_ln<TE>(rows, C, C, m->x, w.ln1_w, w.ln1_b, xn,
+                       hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
+      ++m->launches;
+    }
     // c_attn + KV append
     {
       Epi<TE> e;
@@ -796,6 +800,12 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.T = T;
       e.block = m->block;
       e.pos0 = pos0;
+      if (ln_in) {
+        e.ln_x = m->x;
+        e.ln_ldx = C;
+        e.ln_g = w.ln1_w;
+        e.ln_b = w.ln1_b;
+      }
       int rc;
       if constexpr (kBf16)
         rc = dl ? dec_linear(m, xn, w.attn_w, rows, 3 * C, C, EPI_QKV, e)
@@ -843,14 +853,22 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
         rc = gemm_f32<EPI_RESID>(m, y, w.proj_w, rows, C, C, e);
       if (rc) return rc;
     }
-    // ln_2
-    CK(launch_ln<TE>(rows, C, C, m->x, w.ln2_w, w.ln2_b, xn,
-                     hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
-    ++m->launches;
+    // ln_2 (in the c_fc kernel when ln_in)
+    if (!ln_in) {
+      CK(launch_ln<TE>(rows, C, C, m->x, w.ln2_w, w.ln2_b, xn,
+                       hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
+      ++m->launches;
+    }
     // mlp c_fc + GELU
     {
       Epi<TE> e;
       e.bias = w.fc_b;
+      if (ln_in) {
+        e.ln_x = m->x;
+        e.ln_ldx = C;
+        e.ln_g = w.ln2_w;
+        e.ln_b = w.ln2_b;
+      }
       e.out = hbuf;
       e.out_lo = hilo ? hbuf + static_cast<size_t>(rows) * 4 * C : nullptr;
       e.ldo = 4 * C;
@@ -877,14 +895,24 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       if (rc) return rc;
     }
   }
-  // ln_f on the last position of each sequence, then the tied lm_head
-  CK(launch_ln<TE>(B, C, static_cast<long long>(T) * C, m->x + static_cast<size_t>(T - 1) * C, m->ln_f_w, m->ln_f_b,
-                   xf, kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C, st, pdl));
-  ++m->launches;
+  // ln_f on the last position of each sequence (in the lm_head kernel up to 8 sequences),
+  // then the tied lm_head
+  const bool ln_f_in = kBf16 && B <= DL_LN_MAX_ROWS;
+  if (!ln_f_in) {
+    CK(launch_ln<TE>(B, C, static_cast<long long>(T) * C, m->x + static_cast<size_t>(T - 1) * C, m->ln_f_w,
+                     m->ln_f_b, xf, kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C, st, pdl));
+    ++m->launches;
+  }
   {
     Epi<TE> e;
     e.x = logits;
     e.ldx = V;
+    if (ln_f_in) {
+      e.ln_x = m->x + static_cast<size_t>(T - 1) * C;
+      e.ln_ldx = static_cast<long long>(T) * C;
+      e.ln_g = m->ln_f_w;
+      e.ln_b = m->ln_f_b;
+    }
     int rc;
     if constexpr (kBf16)
       rc = B <= DL_MAX_ROWS ? dec_linear(m, xf, m->wte, B, V, C, EPI_F32, e)
