@@ -112,6 +112,15 @@ void gpt_destroy(gpt_model_t* model);
  * (T > block_size), GPT_ECUDA. */
 int gpt_prefill(gpt_model_t* model, const int32_t* tokens, int32_t B, int32_t T, float* logits);
 
+/* Chunked prefill into the existing cache: append T >= 1 tokens per sequence (tokens: dev,
+ * int32, B x T row-major, B = the batch of the last prefill) at positions cache_len ..
+ * cache_len + T - 1.  Query t attends to keys 0 .. cache_len + t: the causal mask offset by the
+ * cache length (the sketch's `is_causal=(past_kv is None)` is exact only for one new token).
+ * Writes the last new position's logits (dev, fp32, B x vocab_size); the cache length grows by T.
+ * Runs the prefill kernels (tensor-core GEMMs over B x T rows, tiled attention with the offset).
+ * Errors: GPT_ESTATE (no prefill yet), GPT_ECONTEXT (cache length + T > block_size), GPT_EINVAL. */
+int gpt_extend(gpt_model_t* model, const int32_t* tokens, int32_t T, float* logits);
+
 /* One KV-cached step: append token tokens[b] (dev, int32, B = the prefill's batch) at
  * position = current cache length, and write that position's logits (dev, fp32,
  * B x vocab_size).  The cache length grows by one.

@@ -751,10 +751,11 @@ int decode_attn_splits(const gpt_model* m, int B) {
 }
 
 // Enqueue the forward pass over B x T new tokens.  decode: T == 1 and the position comes
-// from m->d_pos; otherwise the tokens start at position 0.  Logits of each sequence's last
-// token go to logits (row stride V).
+// from m->d_pos; otherwise the tokens start at position off (0 for a prefill, the cache
+// length for a chunk appended by gpt_extend, which m->d_pos then holds).  Logits of each
+// sequence's last token go to logits (row stride V).
 template <typename TE>
-int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits) {
+int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off) {
   constexpr bool kBf16 = std::is_same<TE, bf16>::value;
   const int C = m->C, nh = m->nh, V = m->V, rows = B * T;
   const bool hilo = kBf16 && decode && m->hilo_decode;
@@ -763,7 +764,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   // up to 8 rows the decode-shape kernels take LayerNorm(x) as their operand directly
   const bool ln_in = dl && rows <= DL_LN_MAX_ROWS;
   const bool pdl = decode;
-  const int* pos0 = decode ? m->d_pos : nullptr;
+  const int* pos0 = (decode || off > 0) ? m->d_pos : nullptr;
   cudaStream_t st = m->stream;
   TE* xn = static_cast<TE*>(m->xn);
   TE* q = static_cast<TE*>(m->q);
@@ -830,12 +831,14 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
                     static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
                     static_cast<const int*>(m->d_pos), m->ws, m->tickets, y, y_lo, C, m->d_err));
     } else if constexpr (kBf16) {
-      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
+      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, nh, T, m->block, off, y, C);
     } else {
       if (m->hs == 64)
-        attn_prefill_f32<64><<<dim3(T, B * nh), 32, T * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
+        attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, off,
+                                                                                      y, C);
       else
-        attn_prefill_f32<32><<<dim3(T, B * nh), 32, T * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, 0, y, C);
+        attn_prefill_f32<32><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, off,
+                                                                                      y, C);
     }
     CK(cudaGetLastError());
     ++m->launches;
@@ -924,14 +927,14 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   return GPT_OK;
 }
 
-int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits) {
+int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off = 0) {
   m->prof_active = m->prof_enabled && !decode;
   if (m->prof_active) {
     m->prof_n = 0;
     m->prof_flops = 0;
   }
-  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits)
-                         : enqueue_forward<float>(m, tokens, B, T, decode, logits);
+  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off)
+                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off);
   m->prof_active = false;
   return rc;
 }
@@ -1145,6 +1148,20 @@ int gpt_prefill(gpt_model_t* m, const int32_t* tokens, int32_t B, int32_t T, flo
   ++m->launches;
   m->cache_len = T;
   m->batch = B;
+  return GPT_OK;
+}
+
+int gpt_extend(gpt_model_t* m, const int32_t* tokens, int32_t T, float* logits) {
+  if (!m || !tokens || !logits || T < 1) return GPT_EINVAL;
+  if (m->batch < 1) return GPT_ESTATE;
+  if (static_cast<long long>(m->cache_len) + T > m->block) return GPT_ECONTEXT;
+  const int off = m->cache_len;
+  int rc = forward(m, tokens, m->batch, T, false, logits, off);  // d_pos holds the cache length
+  if (rc) return rc;
+  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, off + T, nullptr, 0);
+  CK(cudaGetLastError());
+  ++m->launches;
+  m->cache_len = off + T;
   return GPT_OK;
 }
 

@@ -200,3 +200,53 @@ def test_prefill_gemm_timing_counts_the_linear_layers():
     assert G.gpt_gemm_timing(model.handle)[1] == flops
     G.gpt_profile_gemms(model.handle, False)
     assert model.sync_status() == G.GPT_OK
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_extend_appends_chunks_with_the_offset_mask(dtype):
+    """gpt_extend: chunks appended after a prompt see the cache through the offset causal mask;
+    each chunk's last-position logits equal the oracle's no-cache forward over everything fed,
+    and decode steps continue from the extended cache."""
+    shape = syn.ModelShape(2, 2, 128, 160, 300, True, dtype)
+    sd = syn.make_weights(shape, seed=17, bias_std=0.05, random_gamma=True)
+    cfg, w = oracle_model(shape, sd)
+    B = 3
+    prompt = syn.make_tokens(B, 20, shape.vocab_size, seed=1)
+    chunks = [syn.make_tokens(B, n, shape.vocab_size, seed=10 + n) for n in (7, 1, 30, 64)]
+    model = make_gpu_model(shape, sd, B)
+    tol = F32_TOL if dtype == "f32" else BF16_TOL
+    fed = prompt
+    got = model.prefill(torch.from_numpy(prompt).cuda()).cpu().numpy()
+    assert np.max(np.abs(got - og.forward(cfg, w, fed)[0])) < tol
+    for ch in chunks:
+        fed = np.concatenate([fed, ch], axis=1)
+        got = model.extend(torch.from_numpy(np.ascontiguousarray(ch)).cuda()).cpu().numpy()
+        ref = og.forward(cfg, w, fed)[0]
+        assert np.max(np.abs(got - ref)) < tol, ch.shape
+        assert model.cache_length == fed.shape[1]
+    for step in range(3):  # the decode kernels read the cache the chunks wrote
+        tok = syn.make_tokens(B, 1, shape.vocab_size, seed=40 + step)
+        fed = np.concatenate([fed, tok], axis=1)
+        got = model.decode_step(torch.from_numpy(np.ascontiguousarray(tok[:, 0])).cuda()).cpu().numpy()
+        assert np.max(np.abs(got - og.forward(cfg, w, fed)[0])) < tol
+    assert model.sync_status() == G.GPT_OK
+    model.close()
+
+
+def test_extend_errors():
+    shape = syn.ModelShape(1, 2, 128, 32, 100, False, "bf16")
+    sd = syn.make_weights(shape, seed=2)
+    model = make_gpu_model(shape, sd, 2)
+    toks = torch.from_numpy(syn.make_tokens(2, 8, shape.vocab_size, seed=3)).cuda()
+    with pytest.raises(G.GptError) as ex:
+        model.extend(toks)
+    assert ex.value.code == G.GPT_ESTATE  # no prefill yet
+    model.prefill(toks)
+    model.extend(toks)
+    model.extend(toks)
+    model.extend(toks)  # 32 positions: the cache is full
+    with pytest.raises(G.GptError) as ex:
+        model.extend(toks[:, :1].contiguous())
+    assert ex.value.code == G.GPT_ECONTEXT
+    assert model.cache_length == 32
+    assert model.sync_status() == G.GPT_OK
