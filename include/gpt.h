@@ -133,11 +133,14 @@ int gpt_decode_step(gpt_model_t* model, const int32_t* tokens, float* logits);
  * Sampling: temperature > 0 divides the logits, top_k > 0 keeps the min(top_k, V) largest
  * (ties with the k-th survive), then one draw per row from the softmax by the exact
  * integer inverse CDF with Philox4x64-10 (key = (seed, row), counter = (draw index, 0, 0,
- * 0)); temperature == 0 is greedy argmax (lowest index on ties).  The cache does not
- * slide: T + max_new_tokens - 1 <= block_size is required.
- * The decode steps run as one captured CUDA graph replayed max_new_tokens - 1 times.
+ * 0)); temperature == 0 is greedy argmax (lowest index on ties).
+ * Context: draw j conditions on the last min(T + j, block_size) tokens, as the pages'
+ * generate() crops idx to its last block_size tokens.  While they fit in the cache the draws
+ * run as one captured CUDA graph of a decode step, replayed; past that each draw is a prefill
+ * of the window (positions restart at 0, so nothing can be reused), and a prompt longer than
+ * block_size is cropped the same way.  Afterwards the cache holds the last forward's keys.
  * Errors: GPT_EINVAL (temperature < 0 or not finite, max_new_tokens < 1, B/T as for
- * prefill), GPT_ECONTEXT, GPT_ECUDA. */
+ * prefill), GPT_ECUDA. */
 int gpt_generate(gpt_model_t* model, const int32_t* idx, int32_t B, int32_t T, int32_t max_new_tokens,
                  float temperature, int32_t top_k, uint64_t seed, int32_t* out);
 

@@ -755,7 +755,7 @@ int decode_attn_splits(const gpt_model* m, int B) {
 // length for a chunk appended by gpt_extend, which m->d_pos then holds).  Logits of each
 // sequence's last token go to logits (row stride V).
 template <typename TE>
-int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off) {
+int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off, int tok_ld) {
   constexpr bool kBf16 = std::is_same<TE, bf16>::value;
   const int C = m->C, nh = m->nh, V = m->V, rows = B * T;
   const bool hilo = kBf16 && decode && m->hilo_decode;
@@ -773,7 +773,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   TE* xf = static_cast<TE*>(m->xf);
   const int rows_per_cta = 8;  // 256 threads, warp per row
 
-  embed_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(tokens, rows, T, pos0, static_cast<const TE*>(m->wte),
+  embed_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(tokens, tok_ld, rows, T, pos0, static_cast<const TE*>(m->wte),
                                                                static_cast<const TE*>(m->wpe), V, m->block, C, m->x,
                                                                m->d_err);
   CK(cudaGetLastError());
@@ -927,14 +927,15 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   return GPT_OK;
 }
 
-int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off = 0) {
+int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off = 0, int tok_ld = -1) {
+  if (tok_ld < 0) tok_ld = T;
   m->prof_active = m->prof_enabled && !decode;
   if (m->prof_active) {
     m->prof_n = 0;
     m->prof_flops = 0;
   }
-  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off)
-                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off);
+  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off, tok_ld)
+                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off, tok_ld);
   m->prof_active = false;
   return rc;
 }
@@ -1184,22 +1185,27 @@ int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32
                  int32_t top_k, uint64_t seed, int32_t* out) {
   if (!m || !idx || !out || B < 1 || B > m->Bmax || T < 1 || max_new_tokens < 1) return GPT_EINVAL;
   if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return GPT_EINVAL;
-  if (static_cast<long long>(T) + max_new_tokens - 1 > m->block) return GPT_ECONTEXT;
+  if (static_cast<long long>(T) + max_new_tokens > (1LL << 30)) return GPT_EINVAL;
   const int N = max_new_tokens, W = T + N;
+  // Draw j sees the last min(T + j, block) tokens.  While they fit (T0 + j <= block, T0 the
+  // cropped prompt) the KV cache serves it; after that every draw needs a forward pass over the
+  // window of the last block tokens, whose positions restart at 0, so those run as prefills.
+  const int T0 = std::min(T, m->block);
+  const int n_cached = std::min(N, m->block - T0 + 1);
   m->timing_valid = false;
-  CK(cudaEventRecord(m->ev[0], m->stream));
-  int rc = forward(m, idx, B, T, false, m->logits);
-  if (rc) return rc;
   CK(cudaMemcpy2DAsync(out, W * sizeof(int), idx, T * sizeof(int), T * sizeof(int), B, cudaMemcpyDeviceToDevice,
                        m->stream));
-  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, T, m->d_step, 1);
+  CK(cudaEventRecord(m->ev[0], m->stream));
+  int rc = forward(m, idx + (T - T0), B, T0, false, m->logits, 0, T);
+  if (rc) return rc;
+  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, T0, m->d_step, 1);
   CK(cudaGetLastError());
   ++m->launches;
   if ((rc = enqueue_sample(m, B, temperature, top_k, seed, nullptr, 0, out, W, T, m->stream))) return rc;
   CK(cudaEventRecord(m->ev[1], m->stream));
-  m->cache_len = T;
+  m->cache_len = T0;
   m->batch = B;
-  if (N > 1) {
+  if (n_cached > 1) {
     GraphKey key;
     key.B = B;
     key.T = T;
@@ -1239,11 +1245,23 @@ int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32
       if (ce != cudaSuccess) return cuda_fail(ce, "cudaGraphInstantiate");
       m->gkey = key;
     }
-    for (int j = 1; j < N; ++j) {
+    for (int j = 1; j < n_cached; ++j) {
       CK(cudaGraphLaunch(m->gexec, m->stream));
       m->launches += m->graph_kernels;
     }
-    m->cache_len = T + N - 1;
+    m->cache_len = T0 + n_cached - 1;
+  }
+  // Past the cache: each draw j is a prefill of the window out[:, T + j - block, T + j).
+  for (int j = n_cached; j < N; ++j) {
+    rc = forward(m, out + (T + j - m->block), B, m->block, false, m->logits, 0, W);
+    if (rc) return rc;
+    if ((rc = enqueue_sample(m, B, temperature, top_k, seed, nullptr, j, out, W, T, m->stream))) return rc;
+    m->cache_len = m->block;
+  }
+  if (n_cached < N) {
+    set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, m->block, nullptr, 0);
+    CK(cudaGetLastError());
+    ++m->launches;
   }
   CK(cudaEventRecord(m->ev[2], m->stream));
   m->timing_valid = true;

@@ -12,10 +12,10 @@ namespace kvgpt {
 
 constexpr int LN_MAX_PAIRS = 32;  // up to C = 2048 (C/64 float pairs per lane)
 
-// rows = B*T; row r = b*T + t embeds tokens[r] at position pos0 + t into x[r, :] (fp32).
-// A token outside [0, V) or a position >= block sets the error word and writes zeros.
+// rows = B*T; row r = b*T + t embeds tokens[b * tok_ld + t] at position pos0 + t into x[r, :]
+// (fp32).  A token outside [0, V) or a position >= block sets the error word and writes zeros.
 template <typename TW>
-__global__ void embed_kernel(const int* __restrict__ tokens, int rows, int T, const int* pos0,
+__global__ void embed_kernel(const int* __restrict__ tokens, int tok_ld, int rows, int T, const int* pos0,
                              const TW* __restrict__ wte, const TW* __restrict__ wpe, int V, int block, int C,
                              float* __restrict__ x, int* err) {
   griddep_wait();
@@ -24,7 +24,7 @@ __global__ void embed_kernel(const int* __restrict__ tokens, int rows, int T, co
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
   const int t = r % T;
-  const int tok = tokens[r];
+  const int tok = tokens[static_cast<size_t>(r / T) * tok_ld + t];
   const int pos = (pos0 ? *pos0 : 0) + t;
   float* xr = x + static_cast<size_t>(r) * C;
   const bool bad_tok = tok < 0 || tok >= V;

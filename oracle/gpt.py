@@ -303,3 +303,20 @@ def generate(cfg: Config, w: Weights, idx: np.ndarray, max_new_tokens: int, temp
         if j + 1 < max_new_tokens:
             logits, cache = decode(cfg, w, cache, tok)
     return np.concatenate(out, axis=1)
+
+
+def generate_cropped(cfg: Config, w: Weights, idx: np.ndarray, max_new_tokens: int, temperature: float,
+                     top_k: int | None, seed: int):
+    """[serving] §2 generate() exactly as printed, no cache: before every draw the context is
+    cropped to its last block_size tokens (positions restart at 0 in the window), run through
+    the whole model, and the last position's logits are sampled (draw index j = the step).
+    Agrees with generate() wherever no crop is needed.  Returns (B, T + max_new_tokens) int32."""
+    from oracle import sampler
+
+    idx = np.asarray(idx, dtype=np.int32)
+    for j in range(max_new_tokens):
+        cond = idx if idx.shape[1] <= cfg.block_size else idx[:, -cfg.block_size:]
+        logits = forward(cfg, w, cond)[0]
+        tok = sampler.sample(logits.astype(np.float32), temperature, top_k, seed, j)
+        idx = np.concatenate([idx, tok[:, None].astype(np.int32)], axis=1)
+    return idx

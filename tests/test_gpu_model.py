@@ -163,7 +163,8 @@ def test_error_paths():
     assert G.lib().gpt_decode_step(h, tok.data_ptr(), logits.data_ptr()) == G.GPT_ESTATE
     assert G.lib().gpt_prefill(h, tok.data_ptr(), 3, 4, logits.data_ptr()) == G.GPT_EINVAL  # B > max_batch
     assert G.lib().gpt_prefill(h, tok.data_ptr(), 1, 17, logits.data_ptr()) == G.GPT_ECONTEXT
-    assert G.lib().gpt_generate(h, tok.data_ptr(), 1, 10, 8, 1.0, 0, 0, logits.data_ptr()) == G.GPT_ECONTEXT
+    # past block_size generate crops the context (see the overflow tests); 10 + 8 > 16 is fine
+    assert G.lib().gpt_generate(h, tok.data_ptr(), 1, 10, 8, 1.0, 0, 0, logits.data_ptr()) == G.GPT_OK
     assert G.lib().gpt_generate(h, tok.data_ptr(), 1, 4, 2, float("nan"), 0, 0, logits.data_ptr()) == G.GPT_EINVAL
     # a token id out of range is flagged by the device error word; its embedding row is zeroed
     bad = torch.tensor([[1, 2, 100]], dtype=torch.int32, device="cuda")
@@ -250,3 +251,39 @@ def test_extend_errors():
     assert ex.value.code == G.GPT_ECONTEXT
     assert model.cache_length == 32
     assert model.sync_status() == G.GPT_OK
+
+
+@pytest.mark.parametrize("T,N", [(16, 80), (70, 5)])
+def test_generate_past_block_size_crops_like_the_pages(T, N):
+    """Past block_size every draw sees the last block_size tokens (nanoGPT's crop, positions
+    restarting at 0 in the window): fp32 tiny model, greedy, tokens equal to the oracle's
+    literal generate() loop -- overflow in the middle, and a prompt longer than the block."""
+    wl = syn.WORKLOADS["tiny_b1_p16_d32"]
+    sd = _weights(wl)
+    cfg, w = oracle_model(wl.model, sd)
+    prompt = syn.make_tokens(2, T, 65, seed=7)
+    ref = og.generate_cropped(cfg, w, prompt, N, 0.0, None, 0)
+    model = make_gpu_model(wl.model, sd, 2)
+    out = model.generate(torch.from_numpy(prompt).cuda(), N, temperature=0.0)
+    assert model.sync_status() == G.GPT_OK
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert model.cache_length == cfg.block_size
+
+
+def test_generate_past_block_size_sampled_draws_are_window_prefills():
+    """bf16: each draw past the cache equals the library's own prefill of the last block_size
+    tokens followed by the sampler with that draw's index."""
+    shape = syn.ModelShape(2, 2, 128, 48, 300, True, "bf16")
+    sd = syn.make_weights(shape, seed=23, bias_std=0.02)
+    model = make_gpu_model(shape, sd, 2)
+    prompt = torch.from_numpy(syn.make_tokens(2, 30, 300, seed=5)).cuda()
+    out = model.generate(prompt, 30, temperature=0.9, top_k=40, seed=11).cpu()
+    assert model.sync_status() == G.GPT_OK
+    first_windowed = shape.block_size - 30 + 1  # draws 0..18 run on the cache
+    for j in (first_windowed, first_windowed + 5, 29):
+        window = out[:, 30 + j - shape.block_size:30 + j].contiguous().cuda()
+        logits = model.prefill(window)
+        tok = torch.empty(2, dtype=torch.int32, device="cuda")
+        G.gpt_sample(logits, 0.9, 40, 11, j, tok)
+        assert torch.equal(tok.cpu(), out[:, 30 + j])
+    assert G.gpt_op_status() == G.GPT_OK

@@ -207,3 +207,33 @@ def test_generate_top_k_one_is_greedy_and_cache_bounds():
     og.generate(cfg, w, prompt[:, :4], max_new_tokens=cfg.block_size - 3, temperature=1.0, top_k=5, seed=1)
     with pytest.raises(ValueError):
         og.generate(cfg, w, prompt[:, :4], max_new_tokens=cfg.block_size - 2, temperature=1.0, top_k=5, seed=1)
+
+
+def test_generate_cropped_is_the_cached_generate_until_the_crop():
+    # no crop needed: the pages' generate() without a cache and the cached one draw the same
+    cfg, w, _ = _model(TOY_BIAS, bias_std=0.05)
+    prompt = syn.make_tokens(2, 5, TOY_BIAS.vocab_size, seed=8)
+    n = cfg.block_size - 5 + 1  # the last draw sees exactly block_size tokens
+    a = og.generate(cfg, w, prompt, n, temperature=0.9, top_k=10, seed=4)
+    b = og.generate_cropped(cfg, w, prompt, n, temperature=0.9, top_k=10, seed=4)
+    assert np.array_equal(a, b)
+
+
+def test_generate_cropped_conditions_each_draw_on_the_last_block_size_tokens():
+    # brute force: past the crop, draw j equals the sampler applied to the plain forward of the
+    # last block_size tokens with positions restarting at 0; and a prompt longer than
+    # block_size behaves as its last block_size tokens
+    from oracle import sampler as osm
+
+    cfg, w, _ = _model(TOY, seed=3)
+    bs = cfg.block_size
+    prompt = syn.make_tokens(2, bs - 3, TOY.vocab_size, seed=6)
+    out = og.generate_cropped(cfg, w, prompt, 9, temperature=1.0, top_k=None, seed=2)
+    for j in range(9):
+        ctx = out[:, :prompt.shape[1] + j][:, -bs:]
+        logits = og.forward_full(cfg, w, ctx)[:, -1, :]
+        assert np.array_equal(out[:, prompt.shape[1] + j], osm.sample(logits.astype(np.float32), 1.0, None, 2, j))
+    long_prompt = syn.make_tokens(2, bs + 7, TOY.vocab_size, seed=9)
+    a = og.generate_cropped(cfg, w, long_prompt, 3, temperature=0.0, top_k=None, seed=0)
+    b = og.generate_cropped(cfg, w, long_prompt[:, 7:], 3, temperature=0.0, top_k=None, seed=0)
+    assert np.array_equal(a[:, -3:], b[:, -3:])
