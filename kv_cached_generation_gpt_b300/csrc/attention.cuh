@@ -35,6 +35,8 @@ template <>
 struct Vec8<__nv_bfloat16> {
   uint4 u;
   __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+  // cached rows are read once per step: streaming (evict-first) loads
+  __device__ __forceinline__ void load_stream(const __nv_bfloat16* p) { u = __ldcs(reinterpret_cast<const uint4*>(p)); }
   __device__ __forceinline__ void to_float(float (&f)[8]) const {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -51,6 +53,10 @@ struct Vec8<float> {
   __device__ __forceinline__ void load(const float* p) {
     a = __ldg(reinterpret_cast<const float4*>(p));
     b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void load_stream(const float* p) {
+    a = __ldcs(reinterpret_cast<const float4*>(p));
+    b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
   }
   __device__ __forceinline__ void to_float(float (&f)[8]) const {
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
@@ -115,8 +121,8 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
     for (int u = 0; u < DEC_UNROLL; ++u) {
       const int j = j0 + KPI * u;
       if (j < kend) {
-        kv[u].load(kb + static_cast<size_t>(j) * HSZ);
-        vv[u].load(vb + static_cast<size_t>(j) * HSZ);
+        kv[u].load_stream(kb + static_cast<size_t>(j) * HSZ);
+        vv[u].load_stream(vb + static_cast<size_t>(j) * HSZ);
       }
     }
     float s[DEC_UNROLL];
