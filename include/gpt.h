@@ -112,6 +112,19 @@ void gpt_destroy(gpt_model_t* model);
  * (T > block_size), GPT_ECUDA. */
 int gpt_prefill(gpt_model_t* model, const int32_t* tokens, int32_t B, int32_t T, float* logits);
 
+/* Ragged prefill: sequence b has lengths[b] prompt tokens, the first lengths[b] entries of row b
+ * of tokens (dev, int32, B x T row-major; entries past lengths[b] are ignored), lengths (host,
+ * int32, B) with 1 <= lengths[b] <= T.  Writes each sequence's logits at its own last prompt
+ * position (dev, fp32, B x vocab_size).  Afterwards sequence b's cache length is lengths[b], and
+ * gpt_decode_step appends each sequence's token at its own length (its query sees keys
+ * 0 .. its length); gpt_cache_length reports the longest.  gpt_extend is not available on a
+ * ragged batch (GPT_ESTATE); the next gpt_prefill or gpt_generate ends ragged mode.
+ * Synchronises the model's stream once (the lengths are copied to the device).
+ * Errors: GPT_EINVAL (B, T or a length out of range, NULL pointers), GPT_ECONTEXT
+ * (T > block_size), GPT_ECUDA. */
+int gpt_prefill_ragged(gpt_model_t* model, const int32_t* tokens, const int32_t* lengths, int32_t B, int32_t T,
+                       float* logits);
+
 /* Chunked prefill into the existing cache: append T >= 1 tokens per sequence (tokens: dev,
  * int32, B x T row-major, B = the batch of the last prefill) at positions cache_len ..
  * cache_len + T - 1.  Query t attends to keys 0 .. cache_len + t: the causal mask offset by the
@@ -159,7 +172,8 @@ int gpt_profile_gemms(gpt_model_t* model, int32_t enable);
  * GPT_ESTATE if no prefill was timed. */
 int gpt_gemm_timing(gpt_model_t* model, float* ms, double* flops);
 
-/* Current cache length (host-side mirror), or -1 for NULL. */
+/* Current cache length (host-side mirror; the longest sequence's after a ragged prefill), or -1
+ * for NULL. */
 int32_t gpt_cache_length(const gpt_model_t* model);
 
 /* Number of kernels this model has enqueued since gpt_create (each replay of the decode

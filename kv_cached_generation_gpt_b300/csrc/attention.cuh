@@ -64,7 +64,8 @@ struct Vec8<float> {
   }
 };
 
-// grid (B*nh, splits).  Keys 0..t_len-1 with t_len = *pos0 + 1 are split in chunks of a
+// grid (B*nh, splits).  Keys 0..t_len-1 with t_len = *pos0 + 1 (or pos_rows[b] + 1 when
+// pos_rows is given: sequences of a ragged batch at their own lengths) are split in chunks of a
 // multiple of 16; split s takes [s*chunk, (s+1)*chunk).  ws holds per split (m, l, acc[64])
 // when splits > 1.  y_lo (nullable) receives y - bf16(y).
 // HSZ = head size (32 or 64): LPK = HSZ/8 lanes per key, each holding 8 dims, so a warp
@@ -72,7 +73,8 @@ struct Vec8<float> {
 template <typename T, int HSZ>
 __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __restrict__ q, const T* __restrict__ kc,
                                                                   const T* __restrict__ vc, int nh, int block,
-                                                                  const int* pos0, float* __restrict__ ws,
+                                                                  const int* pos0, const int* pos_rows,
+                                                                  float* __restrict__ ws,
                                                                   unsigned int* __restrict__ tickets,
                                                                   T* __restrict__ y, T* __restrict__ y_lo, int C,
                                                                   int* err) {
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
   const int e = lane % LPK, g = lane / LPK;
   griddep_wait();  // q and the new key/value come from the previous kernel
   griddep_launch();
-  const int t_len = *pos0 + 1;
+  const int t_len = (pos_rows ? pos_rows[bh / nh] : *pos0) + 1;
   if (t_len > block) {
     if (threadIdx.x == 0) atomicOr(err, ERR_POSITION);
     return;

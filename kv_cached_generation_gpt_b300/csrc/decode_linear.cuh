@@ -114,7 +114,7 @@ __device__ __forceinline__ void dl_epilogue8(const Epi<__nv_bfloat16>& e, int r,
     if (part == 0) {
       dst = e.q + (static_cast<size_t>(r) * e.nh + h) * e.hs + d0;
     } else {
-      const int pos = qpos;  // the cache length before this token (read once per thread)
+      const int pos = e.pos_rows ? e.pos_rows[r] : qpos;  // the cache length before this token
       if (pos >= e.block) {
         atomicOr(e.err, ERR_POSITION);
         return;

@@ -49,6 +49,7 @@ struct Epi {
   TE* vc = nullptr;               //          and V cache
   int C = 0, nh = 0, hs = 64, T = 1, block = 0;
   const int* pos0 = nullptr;      // device cache length before the append (null: 0)
+  const int* pos_rows = nullptr;  // or per sequence b: its own cache length (ragged batches)
   float* ws = nullptr;            // split-K partials [splits][M][N]
   unsigned int* tickets = nullptr;
   int splits = 1;
@@ -120,7 +121,7 @@ __device__ __forceinline__ void epi_apply16(const Epi<TE>& e, int r, int n0, flo
     if (part == 0) {
       dst = e.q + ((static_cast<size_t>(b) * e.nh + h) * e.T + t) * e.hs + d0;
     } else {
-      const int pos = (e.pos0 ? *e.pos0 : 0) + t;
+      const int pos = (e.pos_rows ? e.pos_rows[b] : (e.pos0 ? *e.pos0 : 0)) + t;
       if (pos >= e.block) {
         atomicOr(e.err, ERR_POSITION);
         return;

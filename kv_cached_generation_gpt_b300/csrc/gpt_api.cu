@@ -452,6 +452,17 @@ __global__ void set_ints_kernel(int* a, int va, int* b, int vb) {
   if (a) *a = va;
   if (b) *b = vb;
 }
+// x_last[b, :] = x[b * T + lens[b] - 1, :] (each sequence's last prompt row, ragged prefill)
+__global__ void gather_last_kernel(const float* __restrict__ x, const int* __restrict__ lens, int T, int C,
+                                   float* __restrict__ out) {
+  const int b = blockIdx.x;
+  const float* src = x + (static_cast<size_t>(b) * T + lens[b] - 1) * C;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) out[static_cast<size_t>(b) * C + c] = src[c];
+}
+__global__ void add_one_kernel(int* lens, int B) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) lens[b] += 1;
+}
+
 __global__ void advance_kernel(int* pos, int* step) {
   griddep_wait();
   *pos += 1;
@@ -593,6 +604,11 @@ struct gpt_model {
   int* d_pos = nullptr;
   int* d_step = nullptr;
   int* d_tokens = nullptr;
+  // ragged batches (gpt_prefill_ragged): every sequence at its own cache length
+  bool ragged = false;
+  std::vector<int> h_lens;  // host mirror of d_lens
+  int* d_lens = nullptr;
+  float* xlast = nullptr;  // each sequence's last prompt position, gathered for ln_f / lm_head
   int cache_len = 0, batch = 0;
   bool hilo_decode = true;  // hi/lo bf16 operands for decode-step GEMMs (memory-bound, so free)
   cudaGraphExec_t gexec = nullptr;
@@ -755,7 +771,8 @@ int decode_attn_splits(const gpt_model* m, int B) {
 // length for a chunk appended by gpt_extend, which m->d_pos then holds).  Logits of each
 // sequence's last token go to logits (row stride V).
 template <typename TE>
-int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off, int tok_ld) {
+int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off, int tok_ld,
+                    const int* lens) {
   constexpr bool kBf16 = std::is_same<TE, bf16>::value;
   const int C = m->C, nh = m->nh, V = m->V, rows = B * T;
   const bool hilo = kBf16 && decode && m->hilo_decode;
@@ -765,6 +782,9 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   const bool ln_in = dl && rows <= DL_LN_MAX_ROWS;
   const bool pdl = decode;
   const int* pos0 = (decode || off > 0) ? m->d_pos : nullptr;
+  // decode steps of a ragged batch: each sequence at its own length; a ragged prefill: rows
+  // past lens[b] are padding
+  const int* pos_rows = decode && m->ragged ? m->d_lens : nullptr;
   cudaStream_t st = m->stream;
   TE* xn = static_cast<TE*>(m->xn);
   TE* q = static_cast<TE*>(m->q);
@@ -773,7 +793,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   TE* xf = static_cast<TE*>(m->xf);
   const int rows_per_cta = 8;  // 256 threads, warp per row
 
-  embed_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(tokens, tok_ld, rows, T, pos0, static_cast<const TE*>(m->wte),
+  embed_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(tokens, tok_ld, pos_rows, lens, rows, T, pos0, static_cast<const TE*>(m->wte),
                                                                static_cast<const TE*>(m->wpe), V, m->block, C, m->x,
                                                                m->d_err);
   CK(cudaGetLastError());
@@ -801,6 +821,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.T = T;
       e.block = m->block;
       e.pos0 = pos0;
+      e.pos_rows = pos_rows;
       if (ln_in) {
         e.ln_x = m->x;
         e.ln_ldx = C;
@@ -825,11 +846,11 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       if (m->hs == 64)
         CK(launch_k(attn_decode_kernel<TE, 64>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
                     static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
-                    static_cast<const int*>(m->d_pos), m->ws, m->tickets, y, y_lo, C, m->d_err));
+                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
       else
         CK(launch_k(attn_decode_kernel<TE, 32>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
                     static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
-                    static_cast<const int*>(m->d_pos), m->ws, m->tickets, y, y_lo, C, m->d_err));
+                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
     } else if constexpr (kBf16) {
       attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, nh, T, m->block, off, y, C);
     } else {
@@ -899,11 +920,20 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     }
   }
   // ln_f on the last position of each sequence (in the lm_head kernel up to 8 sequences),
-  // then the tied lm_head
+  // then the tied lm_head.  A ragged prefill first gathers each sequence's last prompt row.
+  const float* xlast = m->x + static_cast<size_t>(T - 1) * C;
+  long long xlast_ld = static_cast<long long>(T) * C;
+  if (lens) {
+    gather_last_kernel<<<B, 256, 0, st>>>(m->x, lens, T, C, m->xlast);
+    CK(cudaGetLastError());
+    ++m->launches;
+    xlast = m->xlast;
+    xlast_ld = C;
+  }
   const bool ln_f_in = kBf16 && B <= DL_LN_MAX_ROWS;
   if (!ln_f_in) {
-    CK(launch_ln<TE>(B, C, static_cast<long long>(T) * C, m->x + static_cast<size_t>(T - 1) * C, m->ln_f_w,
-                     m->ln_f_b, xf, kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C, st, pdl));
+    CK(launch_ln<TE>(B, C, xlast_ld, xlast, m->ln_f_w, m->ln_f_b, xf,
+                     kBf16 ? xf + static_cast<size_t>(B) * C : static_cast<TE*>(nullptr), C, st, pdl && !lens));
     ++m->launches;
   }
   {
@@ -911,8 +941,8 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     e.x = logits;
     e.ldx = V;
     if (ln_f_in) {
-      e.ln_x = m->x + static_cast<size_t>(T - 1) * C;
-      e.ln_ldx = static_cast<long long>(T) * C;
+      e.ln_x = xlast;
+      e.ln_ldx = xlast_ld;
       e.ln_g = m->ln_f_w;
       e.ln_b = m->ln_f_b;
     }
@@ -927,15 +957,16 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   return GPT_OK;
 }
 
-int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off = 0, int tok_ld = -1) {
+int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off = 0, int tok_ld = -1,
+            const int* lens = nullptr) {
   if (tok_ld < 0) tok_ld = T;
   m->prof_active = m->prof_enabled && !decode;
   if (m->prof_active) {
     m->prof_n = 0;
     m->prof_flops = 0;
   }
-  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off, tok_ld)
-                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off, tok_ld);
+  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off, tok_ld, lens)
+                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off, tok_ld, lens);
   m->prof_active = false;
   return rc;
 }
@@ -1079,6 +1110,8 @@ int create_impl(const gpt_config_t* cfg, const gpt_weights_t* w, void* stream, g
   m->d_step = m->d_err + 2;
   CK(cudaMemsetAsync(m->d_err, 0, 4 * sizeof(int), m->stream));
   if (!(m->d_tokens = m->alloc<int>(Bm, &rc))) return rc;
+  if (!(m->d_lens = m->alloc<int>(Bm, &rc))) return rc;
+  if (!(m->xlast = m->alloc<float>(Bm * C, &rc))) return rc;
   CK(cudaStreamSynchronize(m->stream));
   return GPT_OK;
 }
@@ -1149,12 +1182,33 @@ int gpt_prefill(gpt_model_t* m, const int32_t* tokens, int32_t B, int32_t T, flo
   ++m->launches;
   m->cache_len = T;
   m->batch = B;
+  m->ragged = false;
+  return GPT_OK;
+}
+
+int gpt_prefill_ragged(gpt_model_t* m, const int32_t* tokens, const int32_t* lengths, int32_t B, int32_t T,
+                       float* logits) {
+  if (!m || !tokens || !lengths || !logits || B < 1 || B > m->Bmax || T < 1) return GPT_EINVAL;
+  if (T > m->block) return GPT_ECONTEXT;
+  int longest = 0;
+  for (int b = 0; b < B; ++b) {
+    if (lengths[b] < 1 || lengths[b] > T) return GPT_EINVAL;
+    longest = std::max(longest, static_cast<int>(lengths[b]));
+  }
+  m->h_lens.assign(lengths, lengths + B);
+  CK(cudaMemcpyAsync(m->d_lens, m->h_lens.data(), B * sizeof(int), cudaMemcpyHostToDevice, m->stream));
+  int rc = forward(m, tokens, B, T, false, logits, 0, T, m->d_lens);
+  if (rc) return rc;
+  CK(cudaStreamSynchronize(m->stream));  // h_lens is the source of the copy above until it lands
+  m->cache_len = longest;
+  m->batch = B;
+  m->ragged = true;
   return GPT_OK;
 }
 
 int gpt_extend(gpt_model_t* m, const int32_t* tokens, int32_t T, float* logits) {
   if (!m || !tokens || !logits || T < 1) return GPT_EINVAL;
-  if (m->batch < 1) return GPT_ESTATE;
+  if (m->batch < 1 || m->ragged) return GPT_ESTATE;
   if (static_cast<long long>(m->cache_len) + T > m->block) return GPT_ECONTEXT;
   const int off = m->cache_len;
   int rc = forward(m, tokens, m->batch, T, false, logits, off);  // d_pos holds the cache length
@@ -1174,7 +1228,12 @@ int gpt_decode_step(gpt_model_t* m, const int32_t* tokens, float* logits) {
   CK(cudaMemcpyAsync(m->d_tokens, tokens, B * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
   int rc = forward(m, m->d_tokens, B, 1, true, logits);
   if (rc) return rc;
-  set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, m->cache_len + 1, nullptr, 0);
+  if (m->ragged) {
+    add_one_kernel<<<1, 128, 0, m->stream>>>(m->d_lens, B);
+    for (int b = 0; b < B; ++b) ++m->h_lens[b];
+  } else {
+    set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, m->cache_len + 1, nullptr, 0);
+  }
   CK(cudaGetLastError());
   ++m->launches;
   m->cache_len += 1;
@@ -1205,6 +1264,7 @@ int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32
   CK(cudaEventRecord(m->ev[1], m->stream));
   m->cache_len = T0;
   m->batch = B;
+  m->ragged = false;
   if (n_cached > 1) {
     GraphKey key;
     key.B = B;
@@ -1468,12 +1528,12 @@ int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache
   if (dtype == GPT_DTYPE_BF16) {
     auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
-                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, c->ws, c->tickets,
+                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
                                        static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, c->err);
   } else {
     auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, c->ws, c->tickets,
+                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
                                        static_cast<float*>(y), nullptr, C, c->err);
   }
   CK(cudaGetLastError());
@@ -1594,12 +1654,12 @@ int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void*
   if (dtype == GPT_DTYPE_BF16) {
     auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
-                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, ws, tickets,
+                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, nullptr, ws, tickets,
                                        static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, err);
   } else {
     auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, ws, tickets,
+                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, nullptr, ws, tickets,
                                        static_cast<float*>(y), nullptr, C, err);
   }
   CK(cudaGetLastError());

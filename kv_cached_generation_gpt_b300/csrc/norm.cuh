@@ -12,10 +12,13 @@ namespace kvgpt {
 
 constexpr int LN_MAX_PAIRS = 32;  // up to C = 2048 (C/64 float pairs per lane)
 
-// rows = B*T; row r = b*T + t embeds tokens[b * tok_ld + t] at position pos0 + t into x[r, :]
-// (fp32).  A token outside [0, V) or a position >= block sets the error word and writes zeros.
+// rows = B*T; row r = b*T + t embeds tokens[b * tok_ld + t] at position pos0 + t (pos_rows[b] + t
+// when pos_rows is given) into x[r, :] (fp32).  With lens, positions t >= lens[b] are padding:
+// zero rows, no check.  A token outside [0, V) or a position >= block sets the error word and
+// writes zeros.
 template <typename TW>
-__global__ void embed_kernel(const int* __restrict__ tokens, int tok_ld, int rows, int T, const int* pos0,
+__global__ void embed_kernel(const int* __restrict__ tokens, int tok_ld, const int* pos_rows, const int* lens,
+                             int rows, int T, const int* pos0,
                              const TW* __restrict__ wte, const TW* __restrict__ wpe, int V, int block, int C,
                              float* __restrict__ x, int* err) {
   griddep_wait();
@@ -23,10 +26,14 @@ __global__ void embed_kernel(const int* __restrict__ tokens, int tok_ld, int row
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
-  const int t = r % T;
-  const int tok = tokens[static_cast<size_t>(r / T) * tok_ld + t];
-  const int pos = (pos0 ? *pos0 : 0) + t;
+  const int t = r % T, b = r / T;
   float* xr = x + static_cast<size_t>(r) * C;
+  if (lens && t >= lens[b]) {
+    for (int c = lane; c < C; c += 32) xr[c] = 0.0f;
+    return;
+  }
+  const int tok = tokens[static_cast<size_t>(b) * tok_ld + t];
+  const int pos = (pos_rows ? pos_rows[b] : (pos0 ? *pos0 : 0)) + t;
   const bool bad_tok = tok < 0 || tok >= V;
   const bool bad_pos = pos >= block;
   if (bad_tok || bad_pos) {

@@ -30,7 +30,7 @@ GPT_DTYPE_F32 = 0
 GPT_DTYPE_BF16 = 1
 
 EXPORTED = (
-    "gpt_create", "gpt_destroy", "gpt_prefill", "gpt_extend", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
+    "gpt_create", "gpt_destroy", "gpt_prefill", "gpt_prefill_ragged", "gpt_extend", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
     "gpt_cache_length", "gpt_kernel_launches", "gpt_sync_status", "gpt_strerror", "gpt_last_error_detail", "gpt_linear_bf16",
     "gpt_layernorm", "gpt_attention_prefill", "gpt_attention_decode", "gpt_sample", "gpt_op_status",
     "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16", "gpt_profile_gemms", "gpt_gemm_timing",
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "gpt_prefill": (ctypes.c_int, [c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
             "gpt_decode_step": (ctypes.c_int, [c_void_p, c_void_p, c_void_p]),
             "gpt_extend": (ctypes.c_int, [c_void_p, c_void_p, c_int32, c_void_p]),
+            "gpt_prefill_ragged": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
             "gpt_generate": (ctypes.c_int, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_float, c_int32,
                                             c_uint64, c_void_p]),
             "gpt_last_timing": (ctypes.c_int, [c_void_p, P(c_float), P(c_float)]),
@@ -173,6 +174,13 @@ def gpt_destroy(model: int) -> None:
 def gpt_prefill(model: int, tokens: torch.Tensor, logits: torch.Tensor) -> None:
     B, T = tokens.shape
     _check(lib().gpt_prefill(model, _ptr(tokens), B, T, _ptr(logits)), "gpt_prefill")
+
+
+def gpt_prefill_ragged(model: int, tokens: torch.Tensor, lengths, logits: torch.Tensor) -> None:
+    """Prefill sequences of different lengths: row b's first lengths[b] tokens (host lengths)."""
+    B, T = tokens.shape
+    lens = (ctypes.c_int32 * B)(*[int(v) for v in lengths])
+    _check(lib().gpt_prefill_ragged(model, _ptr(tokens), lens, B, T, _ptr(logits)), "gpt_prefill_ragged")
 
 
 def gpt_extend(model: int, tokens: torch.Tensor, logits: torch.Tensor) -> None:
@@ -298,6 +306,11 @@ class GPT:
     def prefill(self, tokens: torch.Tensor) -> torch.Tensor:
         logits = torch.empty(tokens.shape[0], self.vocab_size, device=tokens.device, dtype=torch.float32)
         gpt_prefill(self.handle, tokens, logits)
+        return logits
+
+    def prefill_ragged(self, tokens: torch.Tensor, lengths) -> torch.Tensor:
+        logits = torch.empty(tokens.shape[0], self.vocab_size, device=tokens.device)
+        gpt_prefill_ragged(self.handle, tokens, lengths, logits)
         return logits
 
     def extend(self, tokens: torch.Tensor) -> torch.Tensor:

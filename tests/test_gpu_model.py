@@ -287,3 +287,40 @@ def test_generate_past_block_size_sampled_draws_are_window_prefills():
         G.gpt_sample(logits, 0.9, 40, 11, j, tok)
         assert torch.equal(tok.cpu(), out[:, 30 + j])
     assert G.gpt_op_status() == G.GPT_OK
+
+
+@pytest.mark.parametrize("dtype,B", [("bf16", 4), ("bf16", 70), ("f32", 3)])
+def test_ragged_prefill_then_decode_each_sequence_at_its_own_length(dtype, B):
+    """gpt_prefill_ragged: rows of different prompt lengths (padding ids -1, ignored); each
+    row's logits at its own last prompt position, then decode steps appending every row at its
+    own length -- all against the oracle run on each row alone."""
+    shape = syn.ModelShape(2, 2, 128, 64, 300, True, dtype)
+    sd = syn.make_weights(shape, seed=29, bias_std=0.05, random_gamma=True)
+    cfg, w = oracle_model(shape, sd)
+    r = np.random.default_rng(B)
+    T = 30
+    lengths = r.integers(1, T + 1, size=B)
+    lengths[0], lengths[-1] = 1, T
+    tokens = syn.make_tokens(B, T, shape.vocab_size, seed=31)
+    for b in range(B):
+        tokens[b, lengths[b]:] = -1
+    model = make_gpu_model(shape, sd, B)
+    tol = F32_TOL if dtype == "f32" else BF16_TOL
+    seqs = [tokens[b, :lengths[b]] for b in range(B)]
+    got = model.prefill_ragged(torch.from_numpy(tokens).cuda(), lengths).cpu().numpy()
+    ref = np.stack([og.forward(cfg, w, s[None, :])[0][0] for s in seqs])
+    assert np.max(np.abs(got - ref)) < tol
+    assert model.cache_length == T
+    for step in range(4):
+        tok = syn.make_tokens(B, 1, shape.vocab_size, seed=50 + step)[:, 0]
+        seqs = [np.concatenate([s, tok[b:b + 1]]) for b, s in enumerate(seqs)]
+        got = model.decode_step(torch.from_numpy(np.ascontiguousarray(tok)).cuda()).cpu().numpy()
+        ref = np.stack([og.forward(cfg, w, s[None, :])[0][0] for s in seqs])
+        assert np.max(np.abs(got - ref)) < tol, step
+        if dtype != "f32":
+            assert argmax_agreement(got, ref) >= 0.99
+    assert model.sync_status() == G.GPT_OK
+    with pytest.raises(G.GptError) as ex:
+        model.extend(torch.zeros(B, 2, dtype=torch.int32, device="cuda"))
+    assert ex.value.code == G.GPT_ESTATE
+    model.close()
