@@ -192,6 +192,21 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def aggregate_replicas(local: dict, world: int, device) -> dict:
+    """Whole-job times of N independent replicas (one per rank, no exchange on the data path):
+    every timed quantity is the maximum over ranks (the job ends when its slowest replica does);
+    whole-job throughput is then all ranks' units over that time."""
+    if world <= 1:
+        return dict(local)
+    import torch
+    import torch.distributed as dist
+
+    keys = sorted(local)
+    t = torch.tensor([float(local[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return dict(zip(keys, t.tolist()))
+
+
 def workload_config(wl):
     return {"workload": wl.name, "batch": wl.batch, "prompt_tokens": wl.prompt, "decode_steps": wl.decode_steps,
             "temperature": wl.temperature, "top_k": wl.top_k,
@@ -289,12 +304,9 @@ def run_ours(args, rank, world, local_rank):
     if status != G.GPT_OK:
         raise RuntimeError(f"device error word after the timed region: {G.lib().gpt_strerror(status).decode()}")
 
-    dec_s = sum(dec_ms) / 1000.0
-    pre_s = sum(pre_ms) / 1000.0
-    t = torch.tensor([dec_s, pre_s, total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    dec_s, pre_s, total_ms = t.tolist()
+    agg = aggregate_replicas({"decode_s": sum(dec_ms) / 1000.0, "prefill_s": sum(pre_ms) / 1000.0,
+                              "total_ms": total_ms}, world, dev)
+    dec_s, pre_s, total_ms = agg["decode_s"], agg["prefill_s"], agg["total_ms"]
     dec_tokens = world * args.steps * B * (N - 1)
     value = dec_tokens / dec_s
     prefill_tok_s = world * args.steps * B * P / pre_s
