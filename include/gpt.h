@@ -100,6 +100,17 @@ typedef struct gpt_model gpt_model_t;
  * GPT_ECUDA.  On error *out is NULL and nothing stays allocated. */
 int gpt_create(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stream, gpt_model_t** out);
 
+/* gpt_create with a paged KV cache.  Instead of max_batch contiguous caches of block_size
+ * positions, every layer's K and V live in n_pages pages of page_size positions (a power of
+ * two, 64 .. 4096): [layer][k|v][page][head][page_size][head size].  Sequence b's positions
+ * pos map to page table[b][pos / page_size]; the library fills a sequence's table as its cache
+ * grows (gpt_prefill*, gpt_extend, gpt_decode_step, gpt_generate) and every prefill or generate
+ * returns all pages to the pool first.  A call that needs more pages than are free returns
+ * GPT_ENOMEM before anything is enqueued.  Results are identical to the contiguous cache.
+ * Errors: as gpt_create, and GPT_EINVAL for a page_size or n_pages out of range. */
+int gpt_create_paged(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stream, int32_t page_size,
+                     int32_t n_pages, gpt_model_t** out);
+
 /* Release everything gpt_create allocated (synchronises the model's stream first).
  * NULL is a no-op. */
 void gpt_destroy(gpt_model_t* model);

@@ -72,7 +72,8 @@ struct Vec8<float> {
 // covers 32/LPK keys per load instruction.
 template <typename T, int HSZ>
 __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __restrict__ q, const T* __restrict__ kc,
-                                                                  const T* __restrict__ vc, int nh, int block,
+                                                                  const T* __restrict__ vc, KvLayout kv, int nh,
+                                                                  int block,
                                                                   const int* pos0, const int* pos_rows,
                                                                   float* __restrict__ ws,
                                                                   unsigned int* __restrict__ tickets,
@@ -107,8 +108,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
 #pragma unroll
     for (int i = 0; i < 8; ++i) qv[i] *= sc;
   }
-  const T* kb = kc + static_cast<size_t>(bh) * block * HSZ + e * 8;
-  const T* vb = vc + static_cast<size_t>(bh) * block * HSZ + e * 8;
+  const int bq = bh / nh, hq = bh - bq * nh;
 
   float m = -INFINITY, l = 0.0f, acc[8];
 #pragma unroll
@@ -118,20 +118,21 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
   // checks its own key index.
   for (int jb = kbeg + warp * KPW; jb < kend; jb += KPI * DEC_UNROLL) {
     const int j0 = jb + g;
-    Vec8<T> kv[DEC_UNROLL], vv[DEC_UNROLL];
+    Vec8<T> kr[DEC_UNROLL], vv[DEC_UNROLL];
 #pragma unroll
     for (int u = 0; u < DEC_UNROLL; ++u) {
       const int j = j0 + KPI * u;
       if (j < kend) {
-        kv[u].load_stream(kb + static_cast<size_t>(j) * HSZ);
-        vv[u].load_stream(vb + static_cast<size_t>(j) * HSZ);
+        const size_t row = kv.row(bq, hq, j) * HSZ + e * 8;
+        kr[u].load_stream(kc + row);
+        vv[u].load_stream(vc + row);
       }
     }
     float s[DEC_UNROLL];
 #pragma unroll
     for (int u = 0; u < DEC_UNROLL; ++u) {
       float kf[8];
-      kv[u].to_float(kf);
+      kr[u].to_float(kf);
       float d = 0.0f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) d = fmaf(qv[i], kf[i], d);
@@ -269,15 +270,15 @@ __device__ __forceinline__ void cp_async_wait() {
 // Byte offset of 16-byte chunk c of row r in a 64 x 64 bf16 tile with XOR swizzle.
 __device__ __forceinline__ uint32_t swz(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-// Copy rows [row0, row0+ROWS) of a [rows][64] bf16 matrix into a swizzled tile; rows >= nvalid are zeros.
+// Copy ROWS consecutive rows of 64 bf16 starting at src into a swizzled tile; rows >= nvalid are zeros.
 template <int ROWS>
-__device__ __forceinline__ void load_tile64(uint32_t tile, const __nv_bfloat16* src, int row0, int nvalid) {
+__device__ __forceinline__ void load_tile64(uint32_t tile, const __nv_bfloat16* src, int nvalid) {
 #pragma unroll
   for (int i = 0; i < ROWS * 8 / PF_THREADS; ++i) {
     const int idx = threadIdx.x + i * PF_THREADS;  // ROWS x 8 chunks of 16 B
     const int r = idx >> 3, c = idx & 7;
-    const bool ok = row0 + r < nvalid;
-    const __nv_bfloat16* p = src + static_cast<size_t>(ok ? row0 + r : 0) * HS + c * 8;
+    const bool ok = r < nvalid;
+    const __nv_bfloat16* p = src + static_cast<size_t>(ok ? r : 0) * HS + c * 8;
     cp_async16(tile + swz(r, c), p, ok);
   }
 }
@@ -286,7 +287,8 @@ __device__ __forceinline__ void load_tile64(uint32_t tile, const __nv_bfloat16* 
 // Query blocks run heaviest (most keys) first: block qb = gridDim.x - 1 - blockIdx.x.
 __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloat16* __restrict__ q,
                                                                 const __nv_bfloat16* __restrict__ kc,
-                                                                const __nv_bfloat16* __restrict__ vc, int nh, int T,
+                                                                const __nv_bfloat16* __restrict__ vc, KvLayout kv,
+                                                                int nh, int T,
                                                                 int block, int pos0, __nv_bfloat16* __restrict__ y,
                                                                 int C) {
   __shared__ __align__(128) __nv_bfloat16 sQ[PF_BQ * HS];
@@ -300,14 +302,16 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloa
   const int last_key = min(pos0 + q0 + PF_BQ - 1, n_keys - 1);
   const int n_kb = last_key / PF_BKEY + 1;
   const __nv_bfloat16* qg = q + static_cast<size_t>(bh) * T * HS;
-  const __nv_bfloat16* kg = kc + static_cast<size_t>(bh) * block * HS;
-  const __nv_bfloat16* vg = vc + static_cast<size_t>(bh) * block * HS;
+  const int bq = bh / nh, hq = bh - bq * nh;
+  // keys r .. r+63 of this (b, h), r a multiple of 64: consecutive rows (pages hold >= 64)
+  auto krows = [&](int r) { return kc + kv.row(bq, hq, r) * HS; };
+  auto vrows = [&](int r) { return vc + kv.row(bq, hq, r) * HS; };
   constexpr uint32_t TILE_BYTES = PF_BKEY * HS * 2;
   const uint32_t sq = smem_u32(sQ), sk0 = smem_u32(sK[0]), sv0 = smem_u32(sV[0]);
 
-  load_tile64<PF_BQ>(sq, qg, q0, T);
-  load_tile64<PF_BKEY>(sk0, kg, 0, n_keys);
-  load_tile64<PF_BKEY>(sv0, vg, 0, n_keys);
+  load_tile64<PF_BQ>(sq, qg + static_cast<size_t>(q0) * HS, T - q0);
+  load_tile64<PF_BKEY>(sk0, krows(0), n_keys);
+  load_tile64<PF_BKEY>(sv0, vrows(0), n_keys);
   cp_async_commit();
 
   uint32_t qa[4][4];  // A fragments of this warp's 16 query rows, 4 k-steps of 16 dims
@@ -324,8 +328,8 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloa
     const int buf = kb & 1;
     const uint32_t skb = sk0 + buf * TILE_BYTES, svb = sv0 + buf * TILE_BYTES;
     if (kb + 1 < n_kb) {
-      load_tile64<PF_BKEY>(sk0 + (buf ^ 1) * TILE_BYTES, kg, (kb + 1) * PF_BKEY, n_keys);
-      load_tile64<PF_BKEY>(sv0 + (buf ^ 1) * TILE_BYTES, vg, (kb + 1) * PF_BKEY, n_keys);
+      load_tile64<PF_BKEY>(sk0 + (buf ^ 1) * TILE_BYTES, krows((kb + 1) * PF_BKEY), n_keys - (kb + 1) * PF_BKEY);
+      load_tile64<PF_BKEY>(sv0 + (buf ^ 1) * TILE_BYTES, vrows((kb + 1) * PF_BKEY), n_keys - (kb + 1) * PF_BKEY);
     }
     cp_async_commit();
     cp_async_wait<1>();
@@ -447,18 +451,18 @@ __global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloa
 // grid (T, B*nh), 32 threads: one warp per query.  Scores are kept in shared memory.
 template <int HSZ>
 __global__ void attn_prefill_f32(const float* __restrict__ q, const float* __restrict__ kc,
-                                 const float* __restrict__ vc, int nh, int T, int block, int pos0,
+                                 const float* __restrict__ vc, KvLayout kv, int nh, int T, int block, int pos0,
                                  float* __restrict__ y, int C) {
   extern __shared__ float s_p[];  // pos0 + T scores
   const int t = blockIdx.x, bh = blockIdx.y, lane = threadIdx.x;
   const int qp = pos0 + t;
   const float* qr = q + (static_cast<size_t>(bh) * T + t) * HSZ;
-  const float* kg = kc + static_cast<size_t>(bh) * block * HSZ;
-  const float* vg = vc + static_cast<size_t>(bh) * block * HSZ;
+  const int bq = bh / nh, hq = bh - bq * nh;
   float mx = -INFINITY;
   for (int j = lane; j <= qp; j += 32) {
     float d = 0.0f;
-    for (int i = 0; i < HSZ; ++i) d = fmaf(qr[i], kg[static_cast<size_t>(j) * HSZ + i], d);
+    const float* kr = kc + kv.row(bq, hq, j) * HSZ;
+    for (int i = 0; i < HSZ; ++i) d = fmaf(qr[i], kr[i], d);
     d *= (HSZ == 64 ? 0.125f : 0.17677669529663688f);
     s_p[j] = d;
     mx = fmaxf(mx, d);
@@ -475,7 +479,7 @@ __global__ void attn_prefill_f32(const float* __restrict__ q, const float* __res
   const int b = bh / nh, hh = bh - b * nh;
   for (int dd = lane; dd < HSZ; dd += 32) {
     float a = 0.0f;
-    for (int j = 0; j <= qp; ++j) a = fmaf(s_p[j], vg[static_cast<size_t>(j) * HSZ + dd], a);
+    for (int j = 0; j <= qp; ++j) a = fmaf(s_p[j], vc[kv.row(bq, hq, j) * HSZ + dd], a);
     y[(static_cast<size_t>(b) * T + t) * C + hh * HSZ + dd] = a / sum;
   }
 }

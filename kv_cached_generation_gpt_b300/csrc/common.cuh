@@ -245,6 +245,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// ------------------------------------------------------------------ KV cache addressing
+
+// Row (of head-size elements) holding the key or value of sequence b, head h, position pos in
+// one layer's K or V storage: the contiguous cache [b][h][block][hs], or pages
+// [page][h][page_size][hs] found through the sequence's block table (page_size = 2^page_shift,
+// at least 64, so a 64-row tile starting at a multiple of 64 never straddles a page).
+struct KvLayout {
+  int nh = 0, block = 0;
+  const int* table = nullptr;  // [sequence][pages_per_seq] page ids, or null: contiguous
+  int pages_per_seq = 0, page_shift = 0;
+  __device__ __forceinline__ size_t row(int b, int h, int pos) const {
+    if (!table) return (static_cast<size_t>(b) * nh + h) * block + pos;
+    const int pg = max(table[b * pages_per_seq + (pos >> page_shift)], 0);  // the host fills every used entry
+    return ((static_cast<size_t>(pg) * nh + h) << page_shift) + (pos & ((1 << page_shift) - 1));
+  }
+};
+
 // ------------------------------------------------------------------ numerics
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }

@@ -120,7 +120,7 @@ __device__ __forceinline__ void dl_epilogue8(const Epi<__nv_bfloat16>& e, int r,
         return;
       }
       __nv_bfloat16* base = part == 1 ? e.kc : e.vc;
-      dst = base + ((static_cast<size_t>(r) * e.nh + h) * e.block + pos) * e.hs + d0;
+      dst = base + e.kv.row(r, h, pos) * e.hs + d0;
     }
     uint4 o;
     o.x = pack_bf16x2(v[0], v[1]);

@@ -50,6 +50,7 @@ struct Epi {
   int C = 0, nh = 0, hs = 64, T = 1, block = 0;
   const int* pos0 = nullptr;      // device cache length before the append (null: 0)
   const int* pos_rows = nullptr;  // or per sequence b: its own cache length (ragged batches)
+  KvLayout kv;                    // EPI_QKV: where (b, h, pos) lives in kc / vc
   float* ws = nullptr;            // split-K partials [splits][M][N]
   unsigned int* tickets = nullptr;
   int splits = 1;
@@ -127,7 +128,7 @@ __device__ __forceinline__ void epi_apply16(const Epi<TE>& e, int r, int n0, flo
         return;
       }
       TE* base = part == 1 ? e.kc : e.vc;
-      dst = base + ((static_cast<size_t>(b) * e.nh + h) * e.block + pos) * e.hs + d0;
+      dst = base + e.kv.row(b, h, pos) * e.hs + d0;
     }
     store16(dst, v);
   }

@@ -38,6 +38,13 @@ namespace {
 
 thread_local std::string g_detail;
 
+// gpt_create_paged's request, read by gpt_create on the same thread
+struct PagedRequest {
+  bool paged = false;
+  int page_size = 0, n_pages = 0;
+};
+thread_local PagedRequest g_paged_request;
+
 int cuda_fail(cudaError_t e, const char* what) {
   g_detail = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
   return e == cudaErrorMemoryAllocation ? GPT_ENOMEM : GPT_ECUDA;
@@ -641,7 +648,28 @@ struct gpt_model {
   void* vcache(int l) const {
     return static_cast<uint8_t*>(kv) + (static_cast<size_t>(l) * 2 + 1) * cache_layer_bytes();
   }
-  size_t cache_layer_bytes() const { return static_cast<size_t>(Bmax) * nh * block * hs * esz; }
+  size_t cache_layer_bytes() const {
+    return paged ? static_cast<size_t>(n_pages) * nh * page_size * hs * esz
+                 : static_cast<size_t>(Bmax) * nh * block * hs * esz;
+  }
+  // paged KV cache (gpt_create_paged): n_pages pages of page_size positions for every layer's
+  // K and V; sequence b's position pos lives in page h_table[b * pages_per_seq + pos / page_size]
+  bool paged = false;
+  int page_size = 0, page_shift = 0, n_pages = 0, pages_per_seq = 0;
+  int* d_table = nullptr;
+  std::vector<int> h_table;  // -1: no page yet
+  std::vector<int> free_pages;
+  KvLayout kv_layout() const {
+    KvLayout k;
+    k.nh = nh;
+    k.block = block;
+    if (paged) {
+      k.table = d_table;
+      k.pages_per_seq = pages_per_seq;
+      k.page_shift = page_shift;
+    }
+    return k;
+  }
 
   int weight_map(const void* w, long long rows, long long cols, int box_rows, CUtensorMap* out) {
     auto key = std::make_tuple(reinterpret_cast<uintptr_t>(w), rows, cols, box_rows);
@@ -669,6 +697,45 @@ void free_model(gpt_model* m) {
   for (void* p : m->allocs) cudaFree(p);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
   delete m;
+}
+
+// ---- paged KV cache: block tables filled on demand, emptied by every prefill
+
+void release_all_pages(gpt_model* m) {
+  if (!m->paged) return;
+  std::fill(m->h_table.begin(), m->h_table.end(), -1);
+  m->free_pages.clear();
+  for (int pg = m->n_pages - 1; pg >= 0; --pg) m->free_pages.push_back(pg);
+}
+
+// Give sequences 0..B-1 pages for positions < len(b) (len(b) = lens ? lens[b] : len_all), then
+// upload the table (before the kernels that use it are enqueued).  GPT_ENOMEM, before anything
+// is enqueued, when the pool has too few free pages.
+int ensure_pages(gpt_model* m, int B, const int* lens, int len_all) {
+  if (!m->paged) return GPT_OK;
+  size_t need = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = (std::min(lens ? lens[b] : len_all, m->block) + m->page_size - 1) / m->page_size;
+    for (int i = 0; i < n; ++i) need += m->h_table[static_cast<size_t>(b) * m->pages_per_seq + i] < 0;
+  }
+  if (need > m->free_pages.size()) {
+    g_detail = "paged KV cache: " + std::to_string(need) + " more pages needed, " +
+               std::to_string(m->free_pages.size()) + " free";
+    return GPT_ENOMEM;
+  }
+  for (int b = 0; b < B; ++b) {
+    const int n = (std::min(lens ? lens[b] : len_all, m->block) + m->page_size - 1) / m->page_size;
+    for (int i = 0; i < n; ++i) {
+      int& slot = m->h_table[static_cast<size_t>(b) * m->pages_per_seq + i];
+      if (slot < 0) {
+        slot = m->free_pages.back();
+        m->free_pages.pop_back();
+      }
+    }
+  }
+  CK(cudaMemcpyAsync(m->d_table, m->h_table.data(), m->h_table.size() * sizeof(int), cudaMemcpyHostToDevice,
+                     m->stream));
+  return GPT_OK;
 }
 
 // y = A W^T with the given epilogue, bf16 operands.  A has M rows (2M with hilo).
@@ -822,6 +889,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.block = m->block;
       e.pos0 = pos0;
       e.pos_rows = pos_rows;
+      e.kv = m->kv_layout();
       if (ln_in) {
         e.ln_x = m->x;
         e.ln_ldx = C;
@@ -845,20 +913,23 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       // sit on the SMs the c_attn GEMM is still using (measured: 7 % slower decode steps at B=64).
       if (m->hs == 64)
         CK(launch_k(attn_decode_kernel<TE, 64>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
                     static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
       else
         CK(launch_k(attn_decode_kernel<TE, 32>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), nh, m->block,
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
                     static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
     } else if constexpr (kBf16) {
-      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, nh, T, m->block, off, y, C);
+      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, m->kv_layout(), nh, T, m->block,
+                                                                             off, y, C);
     } else {
       if (m->hs == 64)
-        attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, off,
+        attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, m->kv_layout(), nh, T,
+                                                                                      m->block, off,
                                                                                       y, C);
       else
-        attn_prefill_f32<32><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, nh, T, m->block, off,
+        attn_prefill_f32<32><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, m->kv_layout(), nh, T,
+                                                                                      m->block, off,
                                                                                       y, C);
     }
     CK(cudaGetLastError());
@@ -1111,6 +1182,15 @@ int create_impl(const gpt_config_t* cfg, const gpt_weights_t* w, void* stream, g
   CK(cudaMemsetAsync(m->d_err, 0, 4 * sizeof(int), m->stream));
   if (!(m->d_tokens = m->alloc<int>(Bm, &rc))) return rc;
   if (!(m->d_lens = m->alloc<int>(Bm, &rc))) return rc;
+  if (m->paged) {
+    m->pages_per_seq = (m->block + m->page_size - 1) / m->page_size;
+    m->h_table.assign(static_cast<size_t>(Bm) * m->pages_per_seq, -1);
+    if (!(m->d_table = m->alloc<int>(m->h_table.size(), &rc))) return rc;
+    CK(cudaMemcpyAsync(m->d_table, m->h_table.data(), m->h_table.size() * sizeof(int), cudaMemcpyHostToDevice,
+                       m->stream));
+    m->free_pages.clear();
+    for (int pg = m->n_pages - 1; pg >= 0; --pg) m->free_pages.push_back(pg);
+  }
   if (!(m->xlast = m->alloc<float>(Bm * C, &rc))) return rc;
   CK(cudaStreamSynchronize(m->stream));
   return GPT_OK;
@@ -1157,11 +1237,35 @@ int gpt_create(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stre
     if (cfg->bias == 1 ? !all : !none) return GPT_EINVAL;
   }
   gpt_model* m = new gpt_model();
+  if (g_paged_request.paged) {
+    m->paged = true;
+    m->page_size = g_paged_request.page_size;
+    m->n_pages = g_paged_request.n_pages;
+    m->page_shift = 0;
+    while ((1 << m->page_shift) < m->page_size) ++m->page_shift;
+  }
   rc = create_impl(cfg, weights, stream, m);
   if (rc) {
     free_model(m);
     return rc;
   }
+  *out = m;
+  return GPT_OK;
+}
+
+int gpt_create_paged(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stream, int32_t page_size,
+                     int32_t n_pages, gpt_model_t** out) {
+  if (!out) return GPT_EINVAL;
+  *out = nullptr;
+  if (page_size < 64 || page_size > 4096 || (page_size & (page_size - 1)) != 0 || n_pages < 1) return GPT_EINVAL;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  gpt_model_t* m = nullptr;
+  // gpt_create validates the weights; the pool replaces the contiguous cache before it is allocated
+  g_paged_request = {true, page_size, n_pages};
+  rc = gpt_create(cfg, weights, stream, &m);
+  g_paged_request = {};
+  if (rc) return rc;
   *out = m;
   return GPT_OK;
 }
@@ -1175,7 +1279,11 @@ int64_t gpt_kernel_launches(const gpt_model_t* model) { return model ? model->la
 int gpt_prefill(gpt_model_t* m, const int32_t* tokens, int32_t B, int32_t T, float* logits) {
   if (!m || !tokens || !logits || B < 1 || B > m->Bmax || T < 1) return GPT_EINVAL;
   if (T > m->block) return GPT_ECONTEXT;
-  int rc = forward(m, tokens, B, T, false, logits);
+  release_all_pages(m);
+  m->batch = 0;  // until the prefill is enqueued
+  int rc = ensure_pages(m, B, nullptr, T);
+  if (rc) return rc;
+  rc = forward(m, tokens, B, T, false, logits);
   if (rc) return rc;
   set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, T, nullptr, 0);
   CK(cudaGetLastError());
@@ -1196,8 +1304,12 @@ int gpt_prefill_ragged(gpt_model_t* m, const int32_t* tokens, const int32_t* len
     longest = std::max(longest, static_cast<int>(lengths[b]));
   }
   m->h_lens.assign(lengths, lengths + B);
+  release_all_pages(m);
+  m->batch = 0;  // until the prefill is enqueued
+  int rc = ensure_pages(m, B, nullptr, T);  // the padding positions are written too
+  if (rc) return rc;
   CK(cudaMemcpyAsync(m->d_lens, m->h_lens.data(), B * sizeof(int), cudaMemcpyHostToDevice, m->stream));
-  int rc = forward(m, tokens, B, T, false, logits, 0, T, m->d_lens);
+  rc = forward(m, tokens, B, T, false, logits, 0, T, m->d_lens);
   if (rc) return rc;
   CK(cudaStreamSynchronize(m->stream));  // h_lens is the source of the copy above until it lands
   m->cache_len = longest;
@@ -1211,7 +1323,9 @@ int gpt_extend(gpt_model_t* m, const int32_t* tokens, int32_t T, float* logits) 
   if (m->batch < 1 || m->ragged) return GPT_ESTATE;
   if (static_cast<long long>(m->cache_len) + T > m->block) return GPT_ECONTEXT;
   const int off = m->cache_len;
-  int rc = forward(m, tokens, m->batch, T, false, logits, off);  // d_pos holds the cache length
+  int rc = ensure_pages(m, m->batch, nullptr, off + T);
+  if (rc) return rc;
+  rc = forward(m, tokens, m->batch, T, false, logits, off);  // d_pos holds the cache length
   if (rc) return rc;
   set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, off + T, nullptr, 0);
   CK(cudaGetLastError());
@@ -1225,8 +1339,17 @@ int gpt_decode_step(gpt_model_t* m, const int32_t* tokens, float* logits) {
   if (m->batch < 1) return GPT_ESTATE;
   if (m->cache_len + 1 > m->block) return GPT_ECONTEXT;
   const int B = m->batch;
+  int rc;
+  if (m->ragged) {
+    std::vector<int> next(m->h_lens);
+    for (int& v : next) ++v;
+    rc = ensure_pages(m, B, next.data(), 0);
+  } else {
+    rc = ensure_pages(m, B, nullptr, m->cache_len + 1);
+  }
+  if (rc) return rc;
   CK(cudaMemcpyAsync(m->d_tokens, tokens, B * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-  int rc = forward(m, m->d_tokens, B, 1, true, logits);
+  rc = forward(m, m->d_tokens, B, 1, true, logits);
   if (rc) return rc;
   if (m->ragged) {
     add_one_kernel<<<1, 128, 0, m->stream>>>(m->d_lens, B);
@@ -1252,10 +1375,15 @@ int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32
   const int T0 = std::min(T, m->block);
   const int n_cached = std::min(N, m->block - T0 + 1);
   m->timing_valid = false;
+  release_all_pages(m);
+  m->batch = 0;
+  // every position any forward of this call writes: up to T0 + n_cached - 2, or the whole window
+  int rc = ensure_pages(m, B, nullptr, n_cached < N ? m->block : T0 + n_cached - 1);
+  if (rc) return rc;
   CK(cudaMemcpy2DAsync(out, W * sizeof(int), idx, T * sizeof(int), T * sizeof(int), B, cudaMemcpyDeviceToDevice,
                        m->stream));
   CK(cudaEventRecord(m->ev[0], m->stream));
-  int rc = forward(m, idx + (T - T0), B, T0, false, m->logits, 0, T);
+  rc = forward(m, idx + (T - T0), B, T0, false, m->logits, 0, T);
   if (rc) return rc;
   set_ints_kernel<<<1, 1, 0, m->stream>>>(m->d_pos, T0, m->d_step, 1);
   CK(cudaGetLastError());
@@ -1492,16 +1620,19 @@ int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cach
   if (head_size != 64 && !(head_size == 32 && dtype == GPT_DTYPE_F32)) return GPT_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int C = head_size * n_head;
+  KvLayout kvl;
+  kvl.nh = n_head;
+  kvl.block = block;
   if (dtype == GPT_DTYPE_BF16) {
     attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * n_head), PF_THREADS, 0, st>>>(
-        static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache), static_cast<const bf16*>(v_cache), n_head, T,
-        block, pos0, static_cast<bf16*>(y), C);
+        static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache), static_cast<const bf16*>(v_cache), kvl,
+        n_head, T, block, pos0, static_cast<bf16*>(y), C);
   } else if (dtype == GPT_DTYPE_F32) {
     if ((pos0 + T) * sizeof(float) > 48 * 1024) return GPT_EINVAL;
     auto kern = head_size == 64 ? attn_prefill_f32<64> : attn_prefill_f32<32>;
     kern<<<dim3(T, B * n_head), 32, (pos0 + T) * sizeof(float), st>>>(
-        static_cast<const float*>(q), static_cast<const float*>(k_cache), static_cast<const float*>(v_cache), n_head,
-        T, block, pos0, static_cast<float*>(y), C);
+        static_cast<const float*>(q), static_cast<const float*>(k_cache), static_cast<const float*>(v_cache), kvl,
+        n_head, T, block, pos0, static_cast<float*>(y), C);
   } else {
     return GPT_EINVAL;
   }
@@ -1528,12 +1659,12 @@ int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache
   if (dtype == GPT_DTYPE_BF16) {
     auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
-                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
+                                       static_cast<const bf16*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
                                        static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, c->err);
   } else {
     auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
+                                       static_cast<const float*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
                                        static_cast<float*>(y), nullptr, C, c->err);
   }
   CK(cudaGetLastError());
@@ -1654,12 +1785,12 @@ int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void*
   if (dtype == GPT_DTYPE_BF16) {
     auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
-                                       static_cast<const bf16*>(v_cache), n_head, block, pos0_dev, nullptr, ws, tickets,
+                                       static_cast<const bf16*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, ws, tickets,
                                        static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, err);
   } else {
     auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
     kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                       static_cast<const float*>(v_cache), n_head, block, pos0_dev, nullptr, ws, tickets,
+                                       static_cast<const float*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, ws, tickets,
                                        static_cast<float*>(y), nullptr, C, err);
   }
   CK(cudaGetLastError());

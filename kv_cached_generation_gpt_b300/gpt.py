@@ -30,7 +30,7 @@ GPT_DTYPE_F32 = 0
 GPT_DTYPE_BF16 = 1
 
 EXPORTED = (
-    "gpt_create", "gpt_destroy", "gpt_prefill", "gpt_prefill_ragged", "gpt_extend", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
+    "gpt_create", "gpt_create_paged", "gpt_destroy", "gpt_prefill", "gpt_prefill_ragged", "gpt_extend", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
     "gpt_cache_length", "gpt_kernel_launches", "gpt_sync_status", "gpt_strerror", "gpt_last_error_detail", "gpt_linear_bf16",
     "gpt_layernorm", "gpt_attention_prefill", "gpt_attention_decode", "gpt_sample", "gpt_op_status",
     "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16", "gpt_profile_gemms", "gpt_gemm_timing",
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         P = ctypes.POINTER
         sig = {
             "gpt_create": (ctypes.c_int, [P(gpt_config_t), P(gpt_weights_t), c_void_p, P(c_void_p)]),
+            "gpt_create_paged": (ctypes.c_int, [P(gpt_config_t), P(gpt_weights_t), c_void_p, c_int32, c_int32,
+                                                P(c_void_p)]),
             "gpt_destroy": (None, [c_void_p]),
             "gpt_prefill": (ctypes.c_int, [c_void_p, c_void_p, c_int32, c_int32, c_void_p]),
             "gpt_decode_step": (ctypes.c_int, [c_void_p, c_void_p, c_void_p]),
@@ -151,8 +153,10 @@ def _dtype_code(dtype: torch.dtype) -> int:
 
 
 def gpt_create(n_layer: int, n_head: int, n_embd: int, block_size: int, vocab_size: int, bias: bool,
-               dtype: torch.dtype, max_batch: int, state_dict: dict[str, torch.Tensor]) -> int:
-    """Create a model from nanoGPT-named CUDA tensors of ``dtype``; returns the handle."""
+               dtype: torch.dtype, max_batch: int, state_dict: dict[str, torch.Tensor], page_size: int = 0,
+               n_pages: int = 0) -> int:
+    """Create a model from nanoGPT-named CUDA tensors of ``dtype``; returns the handle.  With
+    page_size > 0 the KV cache is a pool of n_pages pages (gpt_create_paged)."""
     cfg = gpt_config_t(n_layer, n_head, n_embd, block_size, vocab_size, 1 if bias else 0, _dtype_code(dtype),
                        max_batch)
     layers = (gpt_layer_weights_t * max(n_layer, 1))()
@@ -163,7 +167,11 @@ def gpt_create(n_layer: int, n_head: int, n_embd: int, block_size: int, vocab_si
                       _ptr(state_dict["transformer.ln_f.weight"]), _ptr(state_dict.get("transformer.ln_f.bias")),
                       layers)
     handle = c_void_p()
-    _check(lib().gpt_create(ctypes.byref(cfg), ctypes.byref(w), _stream(), ctypes.byref(handle)), "gpt_create")
+    if page_size > 0:
+        _check(lib().gpt_create_paged(ctypes.byref(cfg), ctypes.byref(w), _stream(), page_size, n_pages,
+                                      ctypes.byref(handle)), "gpt_create_paged")
+    else:
+        _check(lib().gpt_create(ctypes.byref(cfg), ctypes.byref(w), _stream(), ctypes.byref(handle)), "gpt_create")
     return handle.value
 
 
@@ -299,9 +307,11 @@ def gpt_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache
 class GPT:
     """A model handle plus the buffers the calls need (marshalling only)."""
 
-    def __init__(self, n_layer, n_head, n_embd, block_size, vocab_size, bias, dtype, max_batch, state_dict):
+    def __init__(self, n_layer, n_head, n_embd, block_size, vocab_size, bias, dtype, max_batch, state_dict,
+                 page_size: int = 0, n_pages: int = 0):
         self.vocab_size = vocab_size
-        self.handle = gpt_create(n_layer, n_head, n_embd, block_size, vocab_size, bias, dtype, max_batch, state_dict)
+        self.handle = gpt_create(n_layer, n_head, n_embd, block_size, vocab_size, bias, dtype, max_batch, state_dict,
+                                 page_size, n_pages)
 
     def prefill(self, tokens: torch.Tensor) -> torch.Tensor:
         logits = torch.empty(tokens.shape[0], self.vocab_size, device=tokens.device, dtype=torch.float32)

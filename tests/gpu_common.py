@@ -23,9 +23,10 @@ def oracle_model(shape: syn.ModelShape, sd: dict[str, np.ndarray]):
     return cfg, og.weights_from_state_dict(cfg, syn.storage_values(shape, sd))
 
 
-def make_gpu_model(shape: syn.ModelShape, sd: dict[str, np.ndarray], max_batch: int) -> G.GPT:
+def make_gpu_model(shape: syn.ModelShape, sd: dict[str, np.ndarray], max_batch: int, page_size: int = 0,
+                   n_pages: int = 0) -> G.GPT:
     return G.GPT(shape.n_layer, shape.n_head, shape.n_embd, shape.block_size, shape.vocab_size, shape.bias,
-                 torch_dtype(shape), max_batch, device_state_dict(shape, sd))
+                 torch_dtype(shape), max_batch, device_state_dict(shape, sd), page_size, n_pages)
 
 
 def gpu_teacher_forced(model: G.GPT, prompt: np.ndarray, forced: np.ndarray, rows=None) -> np.ndarray:

@@ -324,3 +324,51 @@ def test_ragged_prefill_then_decode_each_sequence_at_its_own_length(dtype, B):
         model.extend(torch.zeros(B, 2, dtype=torch.int32, device="cuda"))
     assert ex.value.code == G.GPT_ESTATE
     model.close()
+
+
+@pytest.mark.parametrize("dtype,page", [("bf16", 64), ("bf16", 128), ("f32", 64)])
+def test_paged_cache_gives_the_contiguous_results(dtype, page):
+    """gpt_create_paged: the same kernels address the KV rows through block tables, so every
+    logit is bit-identical to the contiguous cache -- prefill, decode steps across page
+    boundaries, a chunk appended with gpt_extend, generate, and a ragged batch."""
+    shape = syn.ModelShape(2, 2, 128, 256, 300, True, dtype)
+    sd = syn.make_weights(shape, seed=37, bias_std=0.05)
+    B = 3
+    flat = make_gpu_model(shape, sd, B)
+    paged = make_gpu_model(shape, sd, B, page_size=page, n_pages=B * (256 // page))
+    prompt = torch.from_numpy(syn.make_tokens(B, 70, 300, seed=2)).cuda()
+    assert torch.equal(flat.prefill(prompt), paged.prefill(prompt))
+    for step in range(70):  # crosses the 128 and 192 page boundaries of page 64
+        tok = torch.from_numpy(syn.make_tokens(B, 1, 300, seed=100 + step)[:, 0].copy()).cuda()
+        assert torch.equal(flat.decode_step(tok), paged.decode_step(tok)), step
+    chunk = torch.from_numpy(syn.make_tokens(B, 20, 300, seed=9)).cuda()
+    assert torch.equal(flat.extend(chunk), paged.extend(chunk))
+    p40 = prompt[:, :40].contiguous()
+    assert torch.equal(flat.generate(p40, 100, temperature=0.8, top_k=30, seed=5),
+                       paged.generate(p40, 100, temperature=0.8, top_k=30, seed=5))
+    lens = [3, 70, 33]
+    assert torch.equal(flat.prefill_ragged(prompt, lens), paged.prefill_ragged(prompt, lens))
+    for step in range(5):
+        tok = torch.from_numpy(syn.make_tokens(B, 1, 300, seed=200 + step)[:, 0].copy()).cuda()
+        assert torch.equal(flat.decode_step(tok), paged.decode_step(tok))
+    assert flat.sync_status() == G.GPT_OK and paged.sync_status() == G.GPT_OK
+
+
+def test_paged_cache_reports_an_exhausted_pool():
+    shape = syn.ModelShape(1, 2, 128, 256, 100, False, "bf16")
+    sd = syn.make_weights(shape, seed=4)
+    model = make_gpu_model(shape, sd, 3, page_size=64, n_pages=3)
+    prompt = torch.from_numpy(syn.make_tokens(3, 70, 100, seed=1)).cuda()
+    with pytest.raises(G.GptError) as ex:
+        model.prefill(prompt)  # 3 sequences x 2 pages > 3 pages
+    assert ex.value.code == G.GPT_ENOMEM
+    model.prefill(prompt[:1].contiguous())  # 2 pages, and the failed call left nothing behind
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(128 - 70):
+        model.decode_step(tok)  # the third page at position 128
+    assert model.cache_length == 128
+    model.decode_step(tok)
+    with pytest.raises(G.GptError) as ex:
+        model.extend(torch.zeros(1, 64, dtype=torch.int32, device="cuda"))  # a fourth page
+    assert ex.value.code == G.GPT_ENOMEM
+    assert model.sync_status() == G.GPT_OK
