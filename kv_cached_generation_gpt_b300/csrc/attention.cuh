@@ -70,7 +70,8 @@ struct Vec8<float> {
 // when splits > 1.  y_lo (nullable) receives y - bf16(y).
 // HSZ = head size (32 or 64): LPK = HSZ/8 lanes per key, each holding 8 dims, so a warp
 // covers 32/LPK keys per load instruction.
-template <typename T, int HSZ>
+// PAGED: the cache rows are found through kv's block table (else kv is the contiguous layout).
+template <typename T, int HSZ, bool PAGED = false>
 __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __restrict__ q, const T* __restrict__ kc,
                                                                   const T* __restrict__ vc, KvLayout kv, int nh,
                                                                   int block,
@@ -109,6 +110,8 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
     for (int i = 0; i < 8; ++i) qv[i] *= sc;
   }
   const int bq = bh / nh, hq = bh - bq * nh;
+  // contiguous cache: the (b, h) rows start here; paged: each key's row through the table
+  const size_t row0 = PAGED ? 0 : (static_cast<size_t>(bq) * kv.nh + hq) * kv.block;
 
   float m = -INFINITY, l = 0.0f, acc[8];
 #pragma unroll
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
     for (int u = 0; u < DEC_UNROLL; ++u) {
       const int j = j0 + KPI * u;
       if (j < kend) {
-        const size_t row = kv.row(bq, hq, j) * HSZ + e * 8;
+        const size_t row = (PAGED ? kv.row(bq, hq, j) : row0 + j) * HSZ + e * 8;
         kr[u].load_stream(kc + row);
         vv[u].load_stream(vc + row);
       }

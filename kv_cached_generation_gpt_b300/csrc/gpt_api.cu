@@ -911,7 +911,15 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       const TE* qc = q;
       // Launched as an ordinary (not programmatic) dependent: its many small CTAs would otherwise
       // sit on the SMs the c_attn GEMM is still using (measured: 7 % slower decode steps at B=64).
-      if (m->hs == 64)
+      if (m->hs == 64 && m->paged)
+        CK(launch_k(attn_decode_kernel<TE, 64, true>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
+                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
+      else if (m->paged)
+        CK(launch_k(attn_decode_kernel<TE, 32, true>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
+                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
+      else if (m->hs == 64)
         CK(launch_k(attn_decode_kernel<TE, 64>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
                     static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
                     static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
