@@ -64,6 +64,18 @@ def prefill_flops(shape, B, P):
     return gemm + attn + head
 
 
+def decode_step_bytes(shape, B, P, steps):
+    """Algorithmic HBM bytes of one decode step, averaged over the workload's steps: every bf16
+    weight read once (the Linear layers and the tied lm_head), the KV cache read up to and
+    including the new position and the new K/V rows written, and the fp32 logits written by the
+    lm_head and read by the sampler.  Step i appends at position P + i."""
+    C, L, V = shape.n_embd, shape.n_layer, shape.vocab_size
+    weights = 2 * (12 * L * C * C + V * C)
+    logits = 2 * B * V * 4
+    kv = sum(2 * L * B * (P + i + 1) * C * 2 + 2 * L * B * C * 2 for i in range(steps)) / steps
+    return weights + kv + logits
+
+
 def decode_attn_bytes(B, nh, hs, t):
     """Algorithmic bytes of one decode-attention launch with t cached keys: K and V rows read
     once, q read, y (hi and lo halves) written, all bf16."""
@@ -390,6 +402,8 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     hbm = pk["hbm_gbs"]
+    step_bytes = decode_step_bytes(shape, B, P, N - 1)
+    step_gbs = step_bytes * args.steps * (N - 1) / dec_s / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -407,6 +421,10 @@ def run_ours(args, rank, world, local_rank):
                          "frac_of_bf16_sustained": gemm_tflops / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
                          "method": "CUDA events around each Linear-layer launch of a 64 x 512 prefill (lm_head "
                                    "excluded), on the model's stream; median of 3"},
+        "decode_step": {"bytes_per_step": step_bytes, "achieved_gbs": step_gbs, "peak_gbs": hbm,
+                        "frac_of_hbm": step_gbs / hbm, "roofline_tok_s": B * hbm * 1e9 / step_bytes,
+                        "note": "weights + KV cache + logits bytes per decode step (mean over the workload's "
+                                "steps) over the measured decode time per step"},
         "decode_b1": {"workload": b1.name, "tok_s": b1_tok_s,
                       "weight_stream_gbs": b1_weight_bytes * b1_tok_s / 1e9,
                       "frac_of_hbm_weights_only": b1_weight_bytes * b1_tok_s / 1e9 / hbm,

@@ -231,6 +231,18 @@ int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out,
 int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
                            int32_t K, int32_t splits, void* stream);
 
+/* The decode-step Linear kernel with the LayerNorm before it fused into its operand:
+ * out (dev, fp32, M x N, row stride N) = LayerNorm(x) W^T (+ bias), eps 1e-5, biased variance,
+ * the normalised rows carried as a bf16 hi/lo pair as in gpt_linear_decode_bf16.  This is how a
+ * decode step of up to 8 sequences runs ln_1 + c_attn, ln_2 + c_fc and ln_f + lm_head
+ * ("nanoGPT 架构分析", §4.1: pre-LN blocks).  Every CTA takes the whole rows' statistics and
+ * normalises its own K-slice.  x (dev, fp32): M rows of K, row r at x + r * x_stride
+ * (x_stride % 4 == 0, 16-byte aligned); 1 <= M <= 8; K <= 2048; gamma (dev, fp32, K); beta
+ * (dev, fp32, K) or NULL; W, bias, splits as in gpt_linear_decode_bf16. */
+int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const float* gamma, const float* beta,
+                                     const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
+                                     int32_t splits, void* stream);
+
 /* y (dev, dtype, rows x C) = LayerNorm(x) with eps 1e-5 and biased variance.
  * x (dev, fp32) row r at x + r * x_stride; gamma (dev, fp32, C); beta (dev, fp32, C) or NULL.
  * y_lo (dev, bf16) or NULL: receives y - bf16(y) (only with dtype == GPT_DTYPE_BF16).

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
   uint64_t* recv_full = acc_full + 1;
   uint64_t* x_full = recv_full + 1;  // [DL_MAX_STAGES]: operand written by warps 0-3 (LayerNorm)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_full + DL_MAX_STAGES);
-  const bool lnx = e.ln_x != nullptr;
+  const bool lnx = e.ln_x != nullptr;  // callers pass LayerNorm inputs only for M <= DL_LN_MAX_ROWS
   __shared__ float s_mean[DL_LN_MAX_ROWS], s_rstd[DL_LN_MAX_ROWS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -277,30 +277,38 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
       asm volatile("bar.sync 1, 128;" ::: "memory");
       // ... then, per k-block, its 64 columns of LN(x) as hi (rows 0..bp-1) and lo (rows
       // bp..2bp-1) in the 128-byte-swizzled layout a TMA load would have written.
+      // Thread t writes the 8-column piece c = t % 8 of row t / 8 (rows past e.M are zeros).
       const int tid = threadIdx.x;
+      const int c = tid & 7;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % stages;
         if (i >= stages && !mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, e.err)) break;
         const uint32_t xt = smem_u32(x_tile(s));
-        for (int it = tid; it < bp * 8; it += 128) {
-          const int r = it >> 3, c = it & 7;
+        const int k = (kb0 + i) * TC_BK + c * 8;
+        float gm[8], bt[8];
+        {
+          const float4 g0 = reinterpret_cast<const float4*>(e.ln_g + k)[0];
+          const float4 g1 = reinterpret_cast<const float4*>(e.ln_g + k)[1];
+          gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
+          gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
+          float4 b0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b1 = b0;
+          if (e.ln_b) {
+            b0 = reinterpret_cast<const float4*>(e.ln_b + k)[0];
+            b1 = reinterpret_cast<const float4*>(e.ln_b + k)[1];
+          }
+          bt[0] = b0.x; bt[1] = b0.y; bt[2] = b0.z; bt[3] = b0.w;
+          bt[4] = b1.x; bt[5] = b1.y; bt[6] = b1.z; bt[7] = b1.w;
+        }
+        const int r = tid >> 3;
+        if (r < bp) {  // bp <= DL_LN_MAX_ROWS: one row per thread
           uint4 hi = make_uint4(0, 0, 0, 0), lo = make_uint4(0, 0, 0, 0);
           if (r < e.M) {
-            const int k = (kb0 + i) * TC_BK + c * 8;
-            const float4* xp = reinterpret_cast<const float4*>(e.ln_x + r * e.ln_ldx + k);
-            const float4* gp = reinterpret_cast<const float4*>(e.ln_g + k);
-            const float4 x0 = xp[0], x1 = xp[1], g0 = gp[0], g1 = gp[1];
+            const float4* xp = reinterpret_cast<const float4*>(e.ln_x + static_cast<size_t>(r) * e.ln_ldx + k);
+            const float4 x0 = xp[0], x1 = xp[1];
             float y[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
             const float mean = s_mean[r], rstd = s_rstd[r];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) y[j] = (y[j] - mean) * rstd * gm[j];
-            if (e.ln_b) {
-              const float4* bp4 = reinterpret_cast<const float4*>(e.ln_b + k);
-              const float4 b0 = bp4[0], b1 = bp4[1];
-              y[0] += b0.x; y[1] += b0.y; y[2] += b0.z; y[3] += b0.w;
-              y[4] += b1.x; y[5] += b1.y; y[6] += b1.z; y[7] += b1.w;
-            }
+            for (int j = 0; j < 8; ++j) y[j] = (y[j] - mean) * rstd * gm[j] + bt[j];
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {

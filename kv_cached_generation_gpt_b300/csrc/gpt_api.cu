@@ -1605,6 +1605,47 @@ int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, floa
   return GPT_OK;
 }
 
+int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const float* gamma, const float* beta,
+                                     const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
+                                     int32_t splits, void* stream) {
+  if (!x || !gamma || !W || !out || M < 1 || M > DL_LN_MAX_ROWS || N < 1 || K < 64 || K % 64 != 0 ||
+      K > 64 * LN_MAX_PAIRS || splits < 0 || x_stride < K || x_stride % 4 != 0)
+    return GPT_EINVAL;
+  const int kb = K / TC_BK;
+  if (splits > 0 && ((splits & (splits - 1)) != 0 || splits > DL_MAX_SPLITS || splits > kb)) return GPT_EINVAL;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return GPT_EUNSUPPORTED;
+  CK(init_dl_attrs(dev));
+  int num_sms = 148;
+  CK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  const int n_tiles = cdiv(N, 128);
+  if (splits == 0) splits = plan_dl_splits(n_tiles, kb, M, num_sms, dev);
+  if (splits > 1 && dl_max_clusters(dev, splits, dl_bp(M), dl_stages(kb, splits)) < 1) {
+    g_detail = std::to_string(splits) + "-CTA clusters of this size cannot be scheduled on this device";
+    return GPT_EUNSUPPORTED;
+  }
+  OpCtx* c = nullptr;
+  int rc = op_ctx(&c, 0, 0);
+  if (rc) return rc;
+  CUtensorMap tw;
+  if ((rc = make_tmap(&tw, W, N, K, 128))) return rc;
+  Epi<bf16> e;
+  e.M = M;
+  e.N = N;
+  e.bias = bias;
+  e.x = out;
+  e.ldx = N;
+  e.err = c->err;
+  e.ln_x = x;
+  e.ln_ldx = x_stride;
+  e.ln_g = gamma;
+  e.ln_b = beta;
+  // the operand is built in shared memory: the activation map is never loaded (W's map stands in)
+  CK(launch_dl(EPI_F32, tw, tw, kb, splits, n_tiles, e, false, static_cast<cudaStream_t>(stream)));
+  return GPT_OK;
+}
+
 int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const float* beta, int32_t rows, int32_t C,
                   int32_t dtype, void* y, void* y_lo, void* stream) {
   if (!x || !gamma || !y || rows < 1 || C < 64 || C % 64 != 0 || C > 64 * LN_MAX_PAIRS || x_stride < C) return GPT_EINVAL;

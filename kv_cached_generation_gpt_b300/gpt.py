@@ -33,7 +33,7 @@ EXPORTED = (
     "gpt_create", "gpt_create_paged", "gpt_destroy", "gpt_prefill", "gpt_prefill_ragged", "gpt_extend", "gpt_decode_step", "gpt_generate", "gpt_last_timing",
     "gpt_cache_length", "gpt_kernel_launches", "gpt_sync_status", "gpt_strerror", "gpt_last_error_detail", "gpt_linear_bf16",
     "gpt_layernorm", "gpt_attention_prefill", "gpt_attention_decode", "gpt_sample", "gpt_op_status",
-    "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16", "gpt_profile_gemms", "gpt_gemm_timing",
+    "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16", "gpt_layernorm_linear_decode_bf16", "gpt_profile_gemms", "gpt_gemm_timing",
 )
 
 c_int32, c_void_p, c_float, c_uint64, c_int64 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float, ctypes.c_uint64, ctypes.c_int64
@@ -103,6 +103,9 @@ def lib() -> ctypes.CDLL:
                                                c_int32, c_int32, c_int32, c_void_p]),
             "gpt_linear_decode_bf16": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                                       c_int32, c_int32, c_void_p]),
+            "gpt_layernorm_linear_decode_bf16": (ctypes.c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
+                                                                 c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                                                 c_int32, c_void_p]),
             "gpt_layernorm": (ctypes.c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                              c_void_p, c_void_p, c_void_p]),
             "gpt_attention_prefill": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
@@ -252,6 +255,16 @@ def gpt_linear_decode_bf16(A: torch.Tensor, W: torch.Tensor, bias: torch.Tensor 
     N, K = W.shape
     _check(lib().gpt_linear_decode_bf16(_ptr(A), _ptr(W), _ptr(bias), _ptr(out), M, N, K, splits, _stream()),
            "gpt_linear_decode_bf16")
+
+
+def gpt_layernorm_linear_decode_bf16(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor | None,
+                                     W: torch.Tensor, bias: torch.Tensor | None, out: torch.Tensor, M: int,
+                                     splits: int = 0, x_stride: int | None = None) -> None:
+    """out = LayerNorm(x[:M]) W^T (+ bias) on the decode-step kernel, the LayerNorm inside it."""
+    N, K = W.shape
+    _check(lib().gpt_layernorm_linear_decode_bf16(_ptr(x), x_stride if x_stride is not None else x.stride(0),
+                                                  _ptr(gamma), _ptr(beta), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                                                  splits, _stream()), "gpt_layernorm_linear_decode_bf16")
 
 
 def gpt_layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor | None, y: torch.Tensor,

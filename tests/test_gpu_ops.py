@@ -152,6 +152,82 @@ def test_linear_decode_rejects_bad_arguments():
             G.gpt_linear_decode_bf16(A, W, None, out, M, splits=splits)
 
 
+# ------------------------------------------------------------------ LayerNorm fused into the decode-step Linear
+
+
+@pytest.mark.parametrize("M,N,K,splits,with_beta", [
+    (1, 256, 768, 4, True),        # ln_1 + c_attn shape at B = 1 (one tile)
+    (1, 2304, 768, 0, False),      # ln_1 + c_attn of GPT-2 124M at B = 1, library-chosen split
+    (3, 3072, 768, 0, True),       # ln_2 + c_fc
+    (8, 2304, 768, 8, True),       # the largest row count of the fused path
+    (5, 50304, 768, 1, False),     # ln_f + lm_head, one CTA per 128-row tile
+    (2, 200, 2048, 16, True),      # the widest rows, 16-CTA clusters, ragged feature tile
+    (7, 130, 320, 2, True),        # 5 k-blocks over 2 CTAs: unequal slices
+])
+def test_layernorm_linear_decode_matches_definition(M, N, K, splits, with_beta):
+    r = _rng(M * 7 + N + K + splits)
+    xs = K + 12                                          # strided rows
+    x = (r.standard_normal((M, xs)) * 1.5 + 3.0).astype(np.float32)  # a mean far from 0
+    g = (1 + 0.1 * r.standard_normal(K)).astype(np.float32)
+    be = (0.1 * r.standard_normal(K)).astype(np.float32) if with_beta else None
+    w = (r.standard_normal((N, K)) * 0.05).astype(np.float32)
+    b = (r.standard_normal(N) * 0.1).astype(np.float32)
+    W = _bf16(w).cuda()
+    xd, gd, bd = torch.from_numpy(x).cuda(), torch.from_numpy(g).cuda(), torch.from_numpy(b).cuda()
+    bed = None if be is None else torch.from_numpy(be).cuda()
+    out = torch.full((M, N), float("nan"), device="cuda")
+    try:
+        G.gpt_layernorm_linear_decode_bf16(xd, gd, bed, W, bd, out, M, splits=splits)
+    except G.GptError as ex:
+        if ex.code == G.GPT_EUNSUPPORTED and splits == 16:
+            pytest.skip("16-CTA clusters cannot be scheduled on this device")
+        raise
+    _ok()
+    y = og.layer_norm(x[:, :K].astype(np.float64), g.astype(np.float64), None if be is None else be.astype(np.float64))
+    ref = og.linear(y, _f64(W), b.astype(np.float64))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    # the normalised operand travels as a bf16 hi/lo pair: ~2^-16 relative per element
+    tol = (2 ** -15 + 8e-6) * math.sqrt(K) * np.max(np.abs(y)) * np.max(np.abs(_f64(W))) + 1e-5
+    assert np.max(np.abs(got - ref)) < tol
+    # the same layer through a separate LayerNorm launch agrees to the same bound
+    yh = torch.empty(M, K, device="cuda", dtype=torch.bfloat16)
+    yl = torch.empty_like(yh)
+    G.gpt_layernorm(xd, gd, bed, yh, yl, x_stride=xs, rows=M)
+    out2 = torch.empty(M, N, device="cuda")
+    try:
+        G.gpt_linear_decode_bf16(torch.cat([yh, yl]), W, bd, out2, M, splits=splits)
+    except G.GptError as ex:
+        if ex.code == G.GPT_EUNSUPPORTED:
+            return
+        raise
+    _ok()
+    assert np.max(np.abs(out2.cpu().numpy().astype(np.float64) - got)) < 2 * tol
+    # deterministic: the partial statistics are merged in split order
+    out3 = torch.empty_like(out)
+    G.gpt_layernorm_linear_decode_bf16(xd, gd, bed, W, bd, out3, M, splits=splits)
+    _ok()
+    assert torch.equal(out.cpu(), out3.cpu())
+
+
+def test_layernorm_linear_decode_rejects_bad_arguments():
+    x = torch.zeros(9, 2112, device="cuda")
+    g = torch.ones(2112, device="cuda")
+    W = torch.zeros(64, 2112, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(9, 64, device="cuda")
+    with pytest.raises(G.GptError):   # whole-row statistics hold at most 2048 columns
+        G.gpt_layernorm_linear_decode_bf16(x, g, None, W, None, out, 8)
+    x2, g2, W2 = x, g[:2048].contiguous(), W[:, :2048].contiguous()  # rows of 2048 at a stride of 2112
+    with pytest.raises(G.GptError):   # more than 8 rows
+        G.gpt_layernorm_linear_decode_bf16(x2, g2, None, W2, None, out, 9, x_stride=2112)
+    with pytest.raises(G.GptError):   # row stride not a multiple of 4 floats
+        G.gpt_layernorm_linear_decode_bf16(x2, g2, None, W2, None, out, 8, x_stride=2049)
+    with pytest.raises(G.GptError):   # splits not a power of two
+        G.gpt_layernorm_linear_decode_bf16(x2, g2, None, W2, None, out, 8, x_stride=2112, splits=3)
+    G.gpt_layernorm_linear_decode_bf16(x2, g2, None, W2, None, out, 8, x_stride=2112)
+    _ok()
+
+
 # ------------------------------------------------------------------ LayerNorm
 
 
