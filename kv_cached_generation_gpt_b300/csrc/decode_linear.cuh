@@ -10,12 +10,13 @@
 // Swap-AB on tcgen05: the weight rows (output features) are the MMA's M = 128 side and the
 // token rows its N side, hi rows then lo rows (N = 2 * Bp, Bp = M rounded up to 8).  One
 // 128-feature tile is split along K across the S CTAs of a thread-block cluster (S <= 16).
-// CTA r owns features [r*128/S, (r+1)*128/S) of the tile.  Each CTA adds the hi and lo
-// halves of its fp32 partial, parks it in shared memory grouped by owner, and after one
-// cluster barrier sends each owner its slice with a bulk shared-to-shared copy (TMA engine,
-// completion counted on the owner's mbarrier).  The owner sums the S slices in split order
-// -- a fixed order, so results do not depend on timing -- and applies the epilogue.  No
-// global scratch is used.
+// CTA r owns features [r*128/S, (r+1)*128/S) of the tile.  TMEM lane f holds feature f for
+// every token row; the thread reading it adds the hi and lo halves and stores the column
+// straight into the owner's shared memory (st.async, counted on the owner's mbarrier; its own
+// slice with plain stores), once a cluster barrier has shown that every CTA's MMAs are done
+// with the ring the receive slots overlay.  The owner sums the S slices in split order -- a
+// fixed order, so results do not depend on timing -- and applies the epilogue.  No global
+// scratch is used.
 //
 // Programmatic dependent launch: weight tiles do not depend on earlier kernels, so they are
 // requested before griddepcontrol.wait; activations, residual and outputs come after it.
@@ -41,17 +42,25 @@ constexpr uint32_t DL_W_BYTES = 128u * TC_BK * 2u;
 
 __host__ __device__ constexpr int dl_bp(int rows) { return (rows + 7) & ~7; }
 __host__ __device__ constexpr uint32_t dl_stage_bytes(int bp) { return DL_W_BYTES + 2u * bp * 128u; }
-// Once the MMAs are done the ring holds the parked partial, S owner slices of bp x R floats
-// each followed by R floats of padding (bp + 1 rows of 128 floats in all), then the receive
-// slots, S x bp x R floats.
-__host__ __device__ constexpr uint32_t dl_park_bytes(int bp) { return static_cast<uint32_t>((bp + 1) * 512); }
+// Once the MMAs are done the ring holds the receive slots: [S][R][bp] floats (sender, feature
+// of the owner's slice, token row), bp x 128 floats in all.  Within a column the 16-byte
+// chunks of 4 rows are XOR-swizzled by the feature (dl_chunk), so that the stores of 8
+// consecutive features fall in distinct banks, and the reduce's reads (a warp covers a few
+// rows x several 8-feature groups) conflict at most 2-way.
+__host__ __device__ constexpr uint32_t dl_recv_bytes(int bp) { return static_cast<uint32_t>(bp * 512); }
 __host__ __device__ constexpr uint32_t dl_ring_bytes(int bp, int stages) {
-  return stages * dl_stage_bytes(bp) > dl_park_bytes(bp) + static_cast<uint32_t>(bp * 512)
-             ? stages * dl_stage_bytes(bp)
-             : dl_park_bytes(bp) + static_cast<uint32_t>(bp * 512);
+  return stages * dl_stage_bytes(bp) > dl_recv_bytes(bp) ? stages * dl_stage_bytes(bp) : dl_recv_bytes(bp);
 }
 __host__ __device__ constexpr uint32_t dl_smem_bytes(int bp, int stages) {
   return 1024u + dl_ring_bytes(bp, stages) + 256u;
+}
+
+// Position of 4-row chunk q in the receive column of feature fr: q ^ ((fr ^ fr / 8) mod g), g
+// the largest power of two <= 8 dividing the chunk count bp / 4 (so the swizzle stays inside
+// the column).
+__device__ __forceinline__ int dl_chunk(int q, int fr, int bp) {
+  const int n = bp >> 2;
+  return q ^ ((fr ^ (fr >> 3)) & (min(8, n & -n) - 1));
 }
 
 // Apply the epilogue to 8 consecutive features n0..n0+7 of token row r (n0 % 8 == 0); qpos is
@@ -131,6 +140,14 @@ __device__ __forceinline__ void dl_epilogue8(const Epi<__nv_bfloat16>& e, int r,
   }
 }
 
+// Bring the global operands of dl_epilogue8 for (row r, features n0..n0+7) into L1.
+template <int EPI>
+__device__ __forceinline__ void dl_prefetch_epilogue(const Epi<__nv_bfloat16>& e, int r, int n0) {
+  if (e.bias) prefetch_l1(e.bias + n0);
+  if (EPI == EPI_RESID) prefetch_l1(e.x + static_cast<size_t>(r) * e.ldx + n0);
+  if (EPI == EPI_QKV && e.pos_rows) prefetch_l1(e.pos_rows + r);
+}
+
 // grid.x = n_tiles * splits, cluster (splits, 1, 1); CTA rank r of cluster c works on
 // feature tile c and k-blocks [r*kb_total/splits, (r+1)*kb_total/splits) (splits <= kb_total),
 // through a ring of `stages` (1..3) shared-memory stages.
@@ -160,10 +177,8 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
   const int kb0 = (rank * kb_total) / splits, kb1 = ((rank + 1) * kb_total) / splits;
   const int nkb = kb1 - kb0;
   const int R = 128 / splits;                  // features owned by each CTA of the cluster
-  const int slice = (bp + 1) * R;              // floats per owner slice in the parked partial
   const uint32_t slice_bytes = static_cast<uint32_t>(bp * R * 4);
-  float* park = reinterpret_cast<float*>(smem);
-  float* recv = reinterpret_cast<float*>(smem + dl_park_bytes(bp));  // [S][bp][R]
+  float* recv = reinterpret_cast<float*>(smem);  // [S][R][bp], over the ring
   uint32_t tcols = 32;
   while (tcols < static_cast<uint32_t>(2 * bp)) tcols <<= 1;
 
@@ -333,13 +348,20 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
         mbar_arrive(&x_full[s]);
       }
     }
-    // Warps 0-3: TMEM lane f = feature f of the tile.  Park hi + lo at park[o][row][f % R] of
-    // owner o = f / R, in the ring: every load into it has landed and every MMA reading it
-    // has completed.
+    // Warps 0-3: TMEM lane f = feature f of the tile, for token rows 0..bp-1 (hi columns, then
+    // lo).  The column goes to recv[rank][f % R][:] of owner o = f / R.
     const bool ok = mbar_wait(acc_full, 0, e.err);
     tc_fence_after();
+    // This CTA's MMAs are done: its ring may take the peers' slices.  The wait below overlaps
+    // the first TMEM load.
+    if (splits > 1) cluster_arrive();
     const int f = warp * 32 + lane;
-    float* dst = park + (f / R) * slice + (f % R);
+    const uint32_t o = static_cast<uint32_t>(f / R);
+    const int fr = f % R;
+    const uint32_t col = smem_u32(recv + (rank * R + fr) * bp);
+    const uint32_t dst = splits > 1 ? mapa_shared(col, o) : col;
+    const uint32_t bar = splits > 1 ? mapa_shared(smem_u32(recv_full), o) : 0u;
+    const bool local = static_cast<int>(o) == rank;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
     for (int c = 0; c < bp; c += 16) {
@@ -353,41 +375,46 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
         tmem_ld8_raw(t_row + bp + c, lo);
       }
       tmem_wait_ld16(hi, lo);
+      if (c == 0 && splits > 1) cluster_wait();  // every CTA of the cluster is past its MMAs
+      float v[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < 8 || two) dst[(c + j) * R] = ok ? __uint_as_float(hi[j]) + __uint_as_float(lo[j]) : 0.0f;
+      for (int j = 0; j < 16; ++j) v[j] = ok ? __uint_as_float(hi[j]) + __uint_as_float(lo[j]) : 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q < 2 || two) {
+          const uint32_t a = dst + static_cast<uint32_t>(dl_chunk((c >> 2) + q, fr, bp) * 16);
+          if (local)
+            st_shared_f4(a, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          else
+            st_async_f4(a, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], bar);
+        }
+      }
     }
-    fence_proxy_async_smem();  // the parked partial is read by bulk copies (async proxy)
   }
   __syncwarp();
   tc_fence_before();
-  if (splits > 1) {
-    // Every CTA of the cluster has finished with its ring: its receive slots may be written.
-    cluster_sync();
-    if (threadIdx.x == 0) {
-      for (int o = 1; o < splits; ++o) {
-        const int to = (rank + o) % splits;
-        const uint32_t dst = mapa_shared(smem_u32(recv + rank * bp * R), static_cast<uint32_t>(to));
-        const uint32_t bar = mapa_shared(smem_u32(recv_full), static_cast<uint32_t>(to));
-        bulk_copy_s2cluster(dst, smem_u32(park + to * slice), slice_bytes, bar);
-      }
-      bulk_commit();
-    }
-    mbar_wait(recv_full, 0, e.err);
-  } else {
-    __syncthreads();
-  }
+  if (splits > 1 && warp >= 4) cluster_sync();  // warps 0-3 met the barrier before sending
+  __syncthreads();                              // this CTA's own slice is written
 
-  // Reduce: this CTA's R features of the tile, for every token row, in split order.
+  // Reduce: this CTA's R features of the tile, for every token row, in split order.  Unit u
+  // is token row u / (R/8) and features fl .. fl+7, fl = 8 (u mod R/8): consecutive threads
+  // cover consecutive features of a row, so the epilogue's stores coalesce.  Its global
+  // operands are fetched into L1 while the peers' slices are still arriving.
   griddep_wait();
   const int upr = R / 8;
   const int units = e.M * upr;
-  int qpos = 0;
-  if (EPI == EPI_QKV && e.pos0) qpos = *e.pos0;
 #pragma unroll 1
   for (int u = threadIdx.x; u < units; u += DL_THREADS) {
-    const int r = u / upr;
-    const int fl = (u - r * upr) * 8;
+    const int r = u / upr, fl = (u - r * upr) * 8;
+    const int n0 = tile * 128 + rank * R + fl;
+    if (n0 < e.N) dl_prefetch_epilogue<EPI>(e, r, n0);
+  }
+  int qpos = 0;
+  if (EPI == EPI_QKV && e.pos0) qpos = *e.pos0;
+  if (splits > 1) mbar_wait(recv_full, 0, e.err);
+#pragma unroll 1
+  for (int u = threadIdx.x; u < units; u += DL_THREADS) {
+    const int r = u / upr, fl = (u - r * upr) * 8;
     const int n0 = tile * 128 + rank * R + fl;
     if (n0 >= e.N) continue;
     float v[8];
@@ -395,16 +422,12 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
     for (int j = 0; j < 8; ++j) v[j] = 0.0f;
 #pragma unroll 1
     for (int s = 0; s < splits; ++s) {
-      const float* src = s == rank ? park + rank * slice + r * R + fl : recv + (s * bp + r) * R + fl;
-      const float4 p0 = reinterpret_cast<const float4*>(src)[0];
-      const float4 p1 = reinterpret_cast<const float4*>(src)[1];
-      v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-      v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+      const float* src = recv + (s * R + fl) * bp + (r & 3);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += src[j * bp + 4 * dl_chunk(r >> 2, fl + j, bp)];
     }
     dl_epilogue8<EPI>(e, r, n0, v, qpos);
   }
-  // The bulk copies out of this CTA's shared memory must have read it before the CTA exits.
-  if (splits > 1 && threadIdx.x == 0) bulk_wait_read();
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
