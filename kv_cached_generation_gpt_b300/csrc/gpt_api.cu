@@ -585,6 +585,9 @@ struct gpt_model {
   gpt_config_t cfg{};
   cudaStream_t stream = nullptr;
   cudaStream_t cap_stream = nullptr;  // private stream used only to record the decode graph
+  // second streams of a decode step that runs as two chains (eager, and while recording)
+  cudaStream_t stream2 = nullptr, cap_stream2 = nullptr;
+  cudaEvent_t ev_mark = nullptr, ev_join = nullptr;
   int dev = 0, num_sms = 148;
   bool bf16 = true;
   size_t esz = 2;
@@ -696,6 +699,10 @@ void free_model(gpt_model* m) {
     if (e) cudaEventDestroy(e);
   for (void* p : m->allocs) cudaFree(p);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  if (m->stream2) cudaStreamDestroy(m->stream2);
+  if (m->cap_stream2) cudaStreamDestroy(m->cap_stream2);
+  if (m->ev_mark) cudaEventDestroy(m->ev_mark);
+  if (m->ev_join) cudaEventDestroy(m->ev_join);
   delete m;
 }
 
@@ -824,13 +831,42 @@ int gemm_f32(gpt_model* m, const float* A, const void* W, int M, int N, int K, E
   return GPT_OK;
 }
 
-int decode_attn_splits(const gpt_model* m, int B) {
+int decode_attn_splits(const gpt_model* m, int B, size_t ws_bytes, size_t n_tickets) {
   const int pairs = B * m->nh;
   int s = cdiv(2 * m->num_sms, pairs);
   s = std::max(1, std::min(s, std::min(32, cdiv(m->block, 16))));
-  while (s > 1 && static_cast<size_t>(pairs) * s * (m->hs + 2) * sizeof(float) > m->ws_bytes) --s;
-  if (static_cast<size_t>(pairs) > m->n_tickets) s = 1;
+  while (s > 1 && static_cast<size_t>(pairs) * s * (m->hs + 2) * sizeof(float) > ws_bytes) --s;
+  if (static_cast<size_t>(pairs) > n_tickets) s = 1;
   return s;
+}
+
+// The sequences [row0, row0 + B) of the batch that one forward pass runs, with the scratch it
+// may use.  A decode step of a large batch runs as two such chains on two streams (see
+// enqueue_decode); everything else runs one chain over the whole batch.
+struct Chain {
+  int row0 = 0;
+  float* x = nullptr;
+  void *xn = nullptr, *q = nullptr, *y = nullptr, *h = nullptr, *xf = nullptr;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  unsigned int* tickets = nullptr;
+  size_t n_tickets = 0;
+  cudaEvent_t mark = nullptr;  // recorded once layer 0's c_attn is enqueued, when set
+};
+
+Chain whole_batch(gpt_model* m) {
+  Chain c;
+  c.x = m->x;
+  c.xn = m->xn;
+  c.q = m->q;
+  c.y = m->y;
+  c.h = m->h;
+  c.xf = m->xf;
+  c.ws = m->ws;
+  c.ws_bytes = m->ws_bytes;
+  c.tickets = m->tickets;
+  c.n_tickets = m->n_tickets;
+  return c;
 }
 
 // Enqueue the forward pass over B x T new tokens.  decode: T == 1 and the position comes
@@ -839,7 +875,7 @@ int decode_attn_splits(const gpt_model* m, int B) {
 // sequence's last token go to logits (row stride V).
 template <typename TE>
 int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* logits, int off, int tok_ld,
-                    const int* lens) {
+                    const int* lens, const Chain& ch) {
   constexpr bool kBf16 = std::is_same<TE, bf16>::value;
   const int C = m->C, nh = m->nh, V = m->V, rows = B * T;
   const bool hilo = kBf16 && decode && m->hilo_decode;
@@ -851,27 +887,36 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   const int* pos0 = (decode || off > 0) ? m->d_pos : nullptr;
   // decode steps of a ragged batch: each sequence at its own length; a ragged prefill: rows
   // past lens[b] are padding
-  const int* pos_rows = decode && m->ragged ? m->d_lens : nullptr;
+  const int* pos_rows = decode && m->ragged ? m->d_lens + ch.row0 : nullptr;
   cudaStream_t st = m->stream;
-  TE* xn = static_cast<TE*>(m->xn);
-  TE* q = static_cast<TE*>(m->q);
-  TE* y = static_cast<TE*>(m->y);
-  TE* hbuf = static_cast<TE*>(m->h);
-  TE* xf = static_cast<TE*>(m->xf);
+  float* x = ch.x;
+  TE* xn = static_cast<TE*>(ch.xn);
+  TE* q = static_cast<TE*>(ch.q);
+  TE* y = static_cast<TE*>(ch.y);
+  TE* hbuf = static_cast<TE*>(ch.h);
+  TE* xf = static_cast<TE*>(ch.xf);
+  // this chain's sequences in the KV cache: an offset into the contiguous cache, or into the
+  // block table
+  KvLayout kvl = m->kv_layout();
+  size_t kv_off = 0;
+  if (m->paged)
+    kvl.table += static_cast<size_t>(ch.row0) * m->pages_per_seq;
+  else
+    kv_off = static_cast<size_t>(ch.row0) * nh * m->block * m->hs;
   const int rows_per_cta = 8;  // 256 threads, warp per row
 
   embed_kernel<TE><<<cdiv(rows, rows_per_cta), 256, 0, st>>>(tokens, tok_ld, pos_rows, lens, rows, T, pos0, static_cast<const TE*>(m->wte),
-                                                               static_cast<const TE*>(m->wpe), V, m->block, C, m->x,
+                                                               static_cast<const TE*>(m->wpe), V, m->block, C, x,
                                                                m->d_err);
   CK(cudaGetLastError());
   ++m->launches;
   for (int l = 0; l < m->L; ++l) {
     const LayerDev& w = m->layers[l];
-    TE* kc = static_cast<TE*>(m->kcache(l));
-    TE* vc = static_cast<TE*>(m->vcache(l));
+    TE* kc = static_cast<TE*>(m->kcache(l)) + kv_off;
+    TE* vc = static_cast<TE*>(m->vcache(l)) + kv_off;
     // ln_1 (in the c_attn kernel when ln_in)
     if (!ln_in) {
-      CK(launch_ln<TE>(rows, C, C, m->x, w.ln1_w, w.ln1_b, xn,
+      CK(launch_ln<TE>(rows, C, C, x, w.ln1_w, w.ln1_b, xn,
                        hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
       ++m->launches;
     }
@@ -889,9 +934,9 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       e.block = m->block;
       e.pos0 = pos0;
       e.pos_rows = pos_rows;
-      e.kv = m->kv_layout();
+      e.kv = kvl;
       if (ln_in) {
-        e.ln_x = m->x;
+        e.ln_x = x;
         e.ln_ldx = C;
         e.ln_g = w.ln1_w;
         e.ln_b = w.ln1_b;
@@ -903,40 +948,41 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       else
         rc = gemm_f32<EPI_QKV>(m, xn, w.attn_w, rows, 3 * C, C, e);
       if (rc) return rc;
+      if (l == 0 && ch.mark) CK(cudaEventRecord(ch.mark, st));
     }
     // attention
     if (decode) {
-      const int splits = decode_attn_splits(m, B);
+      const int splits = decode_attn_splits(m, B, ch.ws_bytes, ch.n_tickets);
       TE* y_lo = hilo ? y + static_cast<size_t>(B) * C : nullptr;
       const TE* qc = q;
       // Launched as an ordinary (not programmatic) dependent: its many small CTAs would otherwise
       // sit on the SMs the c_attn GEMM is still using (measured: 7 % slower decode steps at B=64).
       if (m->hs == 64 && m->paged)
         CK(launch_k(attn_decode_kernel<TE, 64, true>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
+                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
       else if (m->paged)
         CK(launch_k(attn_decode_kernel<TE, 32, true>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
+                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
       else if (m->hs == 64)
         CK(launch_k(attn_decode_kernel<TE, 64>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
+                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
       else
         CK(launch_k(attn_decode_kernel<TE, 32>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), m->kv_layout(), nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, m->ws, m->tickets, y, y_lo, C, m->d_err));
+                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
+                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
     } else if constexpr (kBf16) {
-      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, m->kv_layout(), nh, T, m->block,
+      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, kvl, nh, T, m->block,
                                                                              off, y, C);
     } else {
       if (m->hs == 64)
-        attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, m->kv_layout(), nh, T,
+        attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, kvl, nh, T,
                                                                                       m->block, off,
                                                                                       y, C);
       else
-        attn_prefill_f32<32><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, m->kv_layout(), nh, T,
+        attn_prefill_f32<32><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, kvl, nh, T,
                                                                                       m->block, off,
                                                                                       y, C);
     }
@@ -946,7 +992,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     {
       Epi<TE> e;
       e.bias = w.proj_b;
-      e.x = m->x;
+      e.x = x;
       e.ldx = C;
       int rc;
       if constexpr (kBf16)
@@ -958,7 +1004,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     }
     // ln_2 (in the c_fc kernel when ln_in)
     if (!ln_in) {
-      CK(launch_ln<TE>(rows, C, C, m->x, w.ln2_w, w.ln2_b, xn,
+      CK(launch_ln<TE>(rows, C, C, x, w.ln2_w, w.ln2_b, xn,
                        hilo ? xn + static_cast<size_t>(rows) * C : static_cast<TE*>(nullptr), C, st, pdl));
       ++m->launches;
     }
@@ -967,7 +1013,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       Epi<TE> e;
       e.bias = w.fc_b;
       if (ln_in) {
-        e.ln_x = m->x;
+        e.ln_x = x;
         e.ln_ldx = C;
         e.ln_g = w.ln2_w;
         e.ln_b = w.ln2_b;
@@ -987,7 +1033,7 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
     {
       Epi<TE> e;
       e.bias = w.mproj_b;
-      e.x = m->x;
+      e.x = x;
       e.ldx = C;
       int rc;
       if constexpr (kBf16)
@@ -1000,10 +1046,10 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
   }
   // ln_f on the last position of each sequence (in the lm_head kernel up to 8 sequences),
   // then the tied lm_head.  A ragged prefill first gathers each sequence's last prompt row.
-  const float* xlast = m->x + static_cast<size_t>(T - 1) * C;
+  const float* xlast = x + static_cast<size_t>(T - 1) * C;
   long long xlast_ld = static_cast<long long>(T) * C;
   if (lens) {
-    gather_last_kernel<<<B, 256, 0, st>>>(m->x, lens, T, C, m->xlast);
+    gather_last_kernel<<<B, 256, 0, st>>>(x, lens, T, C, m->xlast);
     CK(cudaGetLastError());
     ++m->launches;
     xlast = m->xlast;
@@ -1044,14 +1090,60 @@ int forward(gpt_model* m, const int* tokens, int B, int T, bool decode, float* l
     m->prof_n = 0;
     m->prof_flops = 0;
   }
-  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off, tok_ld, lens)
-                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off, tok_ld, lens);
+  const Chain ch = whole_batch(m);
+  const int rc = m->bf16 ? enqueue_forward<bf16>(m, tokens, B, T, decode, logits, off, tok_ld, lens, ch)
+                         : enqueue_forward<float>(m, tokens, B, T, decode, logits, off, tok_ld, lens, ch);
   m->prof_active = false;
   return rc;
 }
 
+// A decode step over B sequences (tokens: B ids).  From DECODE_TWO_CHAINS_MIN sequences up
+// (bf16, decode-shape kernels) it runs as two chains of about B/2 sequences on two streams,
+// the second starting once the first has enqueued layer 0's c_attn.  The kernels of one chain
+// are latency-bound (the decode Linear layers and LayerNorms of a few dozen rows) while the
+// other chain's attention streams its share of the KV cache, so the two overlap; each chain
+// has its own rows of every scratch buffer and its own half of the split-KV scratch.  Both
+// chains are joined on the model's stream before this returns.
+constexpr int DECODE_TWO_CHAINS_MIN = 32;
+
+bool decode_two_chains(const gpt_model* m, int B) {
+  return m->bf16 && m->hilo_decode && B >= DECODE_TWO_CHAINS_MIN && B <= DL_MAX_ROWS;
+}
+
+int decode_forward(gpt_model* m, const int* tokens, int B, float* logits) {
+  if (!decode_two_chains(m, B)) return forward(m, tokens, B, 1, true, logits);
+  m->prof_active = false;
+  const int B0 = B / 2, B1 = B - B0;
+  const size_t C = m->C, e = m->esz;
+  const cudaStream_t s1 = m->stream;
+  const cudaStream_t s2 = s1 == m->cap_stream ? m->cap_stream2 : m->stream2;
+  Chain a = whole_batch(m), b = whole_batch(m);
+  a.mark = m->ev_mark;
+  a.ws_bytes = b.ws_bytes = (m->ws_bytes / 2) & ~static_cast<size_t>(255);
+  a.n_tickets = b.n_tickets = m->n_tickets / 2;
+  b.row0 = B0;
+  b.x = m->x + B0 * C;
+  b.xn = static_cast<uint8_t*>(m->xn) + 2 * B0 * C * e;  // hi and lo rows of chain a come first
+  b.q = static_cast<uint8_t*>(m->q) + B0 * C * e;
+  b.y = static_cast<uint8_t*>(m->y) + 2 * B0 * C * e;
+  b.h = static_cast<uint8_t*>(m->h) + 2 * B0 * 4 * C * e;
+  b.xf = static_cast<uint8_t*>(m->xf) + 2 * B0 * C * e;
+  b.ws = m->ws + a.ws_bytes / sizeof(float);
+  b.tickets = m->tickets + a.n_tickets;
+  int rc = enqueue_forward<bf16>(m, tokens, B0, 1, true, logits, 0, 1, nullptr, a);
+  if (rc) return rc;
+  CK(cudaStreamWaitEvent(s2, m->ev_mark, 0));
+  m->stream = s2;
+  rc = enqueue_forward<bf16>(m, tokens + B0, B1, 1, true, logits + static_cast<size_t>(B0) * m->V, 0, 1, nullptr, b);
+  m->stream = s1;
+  if (rc) return rc;
+  CK(cudaEventRecord(m->ev_join, s2));
+  CK(cudaStreamWaitEvent(s1, m->ev_join, 0));
+  return GPT_OK;
+}
+
 int enqueue_sample(gpt_model* m, int B, float temperature, int top_k, unsigned long long seed, const int* step_dev,
-                   int step, int* out, int out_stride, int out_col0, cudaStream_t st) {
+                   int step, int* out, int out_stride, int out_col0, cudaStream_t st, bool pdl = true) {
   CK(set_sampler_smem(m->dev, m->V));
   SampleArgs a;
   a.logits = m->logits;
@@ -1069,7 +1161,7 @@ int enqueue_sample(gpt_model* m, int B, float temperature, int top_k, unsigned l
   a.thr_out = nullptr;
   a.w_out = nullptr;
   a.cand_cap = sampler_cand_cap(m->V);
-  CK(launch_k(sample_kernel, dim3(B), dim3(SMP_THREADS), sampler_smem(m->V), st, true, a));
+  CK(launch_k(sample_kernel, dim3(B), dim3(SMP_THREADS), sampler_smem(m->V), st, pdl, a));
   ++m->launches;
   return GPT_OK;
 }
@@ -1130,6 +1222,10 @@ int create_impl(const gpt_config_t* cfg, const gpt_weights_t* w, void* stream, g
   CK(init_kernel_attrs(m->dev));
   CK(set_sampler_smem(m->dev, cfg->vocab_size));
   CK(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking));
+  CK(cudaStreamCreateWithFlags(&m->stream2, cudaStreamNonBlocking));
+  CK(cudaStreamCreateWithFlags(&m->cap_stream2, cudaStreamNonBlocking));
+  CK(cudaEventCreateWithFlags(&m->ev_mark, cudaEventDisableTiming));
+  CK(cudaEventCreateWithFlags(&m->ev_join, cudaEventDisableTiming));
   for (auto& e : m->ev) CK(cudaEventCreate(&e));
   m->bf16 = cfg->dtype == GPT_DTYPE_BF16;
   m->esz = m->bf16 ? 2 : 4;
@@ -1357,7 +1453,7 @@ int gpt_decode_step(gpt_model_t* m, const int32_t* tokens, float* logits) {
   }
   if (rc) return rc;
   CK(cudaMemcpyAsync(m->d_tokens, tokens, B * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-  rc = forward(m, m->d_tokens, B, 1, true, logits);
+  rc = decode_forward(m, m->d_tokens, B, logits);
   if (rc) return rc;
   if (m->ragged) {
     add_one_kernel<<<1, 128, 0, m->stream>>>(m->d_lens, B);
@@ -1419,8 +1515,11 @@ int gpt_generate(gpt_model_t* m, const int32_t* idx, int32_t B, int32_t T, int32
       const long long launches0 = m->launches;
       m->stream = m->cap_stream;
       CK(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
-      rc = forward(m, m->d_tokens, B, 1, true, m->logits);
-      if (!rc) rc = enqueue_sample(m, B, temperature, top_k, seed, m->d_step, 0, out, W, T, m->cap_stream);
+      rc = decode_forward(m, m->d_tokens, B, m->logits);
+      // after a join of two chains the sampler is an ordinary dependent
+      if (!rc)
+        rc = enqueue_sample(m, B, temperature, top_k, seed, m->d_step, 0, out, W, T, m->cap_stream,
+                            !decode_two_chains(m, B));
       if (!rc) {
         if (launch_k(advance_kernel, dim3(1), dim3(1), 0, m->cap_stream, true, m->d_pos, m->d_step) != cudaSuccess)
           rc = GPT_ECUDA;
