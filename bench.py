@@ -39,6 +39,9 @@ if ROOT not in sys.path:
 METRIC = "GPT-2 124M KV-cache decode tok/s (B=1,64), prefill tok/s, % HBM/TC roofline"
 WORKLOAD = "gpt2_124m_b64_p512_d512"
 B1_WORKLOAD = "gpt2_124m_b1_p128_d896"
+# char-level model (21 MB of weights: L2-resident, the HBM fraction is nominal) and the
+# 350M-shape model with biases
+SECONDARY_WORKLOADS = ("char_b1_p1_d255", "gpt2_350m_b8_p768_d256")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 ATTN_PROFILE = os.path.join(ROOT, "profiles", "attn_decode_b64_gpt2_124m.md")
@@ -74,6 +77,41 @@ def decode_step_bytes(shape, B, P, steps):
     logits = 2 * B * V * 4
     kv = sum(2 * L * B * (P + i + 1) * C * 2 + 2 * L * B * C * 2 for i in range(steps)) / steps
     return weights + kv + logits
+
+
+def secondary_workload(G, syn, name, dev, seed, hbm):
+    """Prefill and decode rates of another configuration of the survey's measurement table
+    (one gpt_generate per run: a prefill of the prompt, then the workload's decode steps;
+    median of 3 runs after one warm-up), with the decode step's fraction of the HBM roofline."""
+    import torch
+
+    wl = syn.WORKLOADS[name]
+    shape = wl.model
+    sd = {k: torch.from_numpy(v).to(torch.bfloat16).to(dev)
+          for k, v in syn.make_weights(shape, bias_std=wl.bias_std).items()}
+    model = G.GPT(shape.n_layer, shape.n_head, shape.n_embd, shape.block_size, shape.vocab_size, shape.bias,
+                  torch.bfloat16, wl.batch, sd)
+    del sd
+    prompt = torch.from_numpy(syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)).to(dev)
+    N = wl.decode_steps + 1
+    out = torch.empty(wl.batch, wl.prompt + N, dtype=torch.int32, device=dev)
+    pre, dec = [], []
+    for i in range(4):
+        G.gpt_generate(model.handle, prompt, N, wl.temperature, wl.top_k, seed, out)
+        a, b = G.gpt_last_timing(model.handle)
+        if i >= 1:
+            pre.append(a)
+            dec.append(b)
+    if model.sync_status() != G.GPT_OK:
+        raise RuntimeError(f"device error word after {name}")
+    model.close()
+    step_s = statistics.median(dec) / 1000.0 / wl.decode_steps
+    step_bytes = decode_step_bytes(shape, wl.batch, wl.prompt, wl.decode_steps)
+    return {"workload": name, "prefill_tok_s": wl.batch * wl.prompt / (statistics.median(pre) / 1000.0),
+            "prefill_tflops": prefill_flops(shape, wl.batch, wl.prompt) / (statistics.median(pre) / 1000.0) / 1e12,
+            "decode_tok_s": wl.batch / step_s, "decode_step_us": step_s * 1e6,
+            "decode_frac_of_hbm": step_bytes / step_s / 1e9 / hbm,
+            "decode_bytes_per_step": step_bytes}
 
 
 def decode_attn_bytes(B, nh, hs, t):
@@ -367,6 +405,12 @@ def run_ours(args, rank, world, local_rank):
     b1_tok_s = b1.decode_steps / (statistics.median(b1_dec) / 1000.0)
     b1_weight_bytes = 2 * (12 * shape.n_layer * shape.n_embd ** 2 + shape.vocab_size * shape.n_embd)
 
+    # ---- the other configurations of the measurement table (rank 0 only)
+    secondary = []
+    if rank == 0:
+        for name in SECONDARY_WORKLOADS:
+            secondary.append(secondary_workload(G, syn, name, dev, seed, pk["hbm_gbs"]))
+
     # ---- dominant kernel: decode attention, one launch per cache length of the workload
     nh, hs = shape.n_head, shape.n_embd // shape.n_head
     kc = torch.randn(B, nh, shape.block_size, hs, device=dev).to(torch.bfloat16)
@@ -425,6 +469,7 @@ def run_ours(args, rank, world, local_rank):
                         "frac_of_hbm": step_gbs / hbm, "roofline_tok_s": B * hbm * 1e9 / step_bytes,
                         "note": "weights + KV cache + logits bytes per decode step (mean over the workload's "
                                 "steps) over the measured decode time per step"},
+        "secondary": secondary,
         "decode_b1": {"workload": b1.name, "tok_s": b1_tok_s,
                       "weight_stream_gbs": b1_weight_bytes * b1_tok_s / 1e9,
                       "frac_of_hbm_weights_only": b1_weight_bytes * b1_tok_s / 1e9 / hbm,
