@@ -284,8 +284,6 @@ cudaError_t set_tc_attr(int bn, bool hilo, int epi, int dev) {
 // each cluster size (2, 4, 8, 16), token-row class (bp = 8 .. 128) and stage count (1 .. 3).
 // Filled once per device (outside any stream capture); plans keep a launch within one wave.
 int g_dl_max_clusters[64][5][DL_MAX_ROWS / 8][DL_MAX_STAGES] = {};
-// ... and how many single CTAs per SM (no cluster), per token-row class and stage count.
-int g_dl_max_blocks[64][DL_MAX_ROWS / 8][DL_MAX_STAGES] = {};
 unsigned long long g_dl_attr_mask = 0;
 std::mutex g_dl_mu;
 
@@ -333,15 +331,6 @@ cudaError_t init_dl_attrs(int dev) {
           n = 0;
         }
         g_dl_max_clusters[dev][si][bi][st - 1] = n;
-        if (si == 0) {
-          int nb = 0;
-          if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, dec_linear_kernel<EPI_RESID>, DL_THREADS,
-                                                            dl_smem_bytes(8 * (bi + 1), st)) != cudaSuccess) {
-            cudaGetLastError();
-            nb = 0;
-          }
-          g_dl_max_blocks[dev][bi][st - 1] = nb;
-        }
       }
   g_dl_attr_mask |= 1ull << dev;
   return cudaSuccess;
@@ -349,19 +338,6 @@ cudaError_t init_dl_attrs(int dev) {
 
 int dl_stages(int kb, int splits) { return std::min(DL_MAX_STAGES, cdiv(kb, splits)); }
 
-// Ring stages of a launch: dl_stages, except that an unsplit grid too large for one wave at 3
-// stages takes 2 when that fits it in one wave (a large lm_head: 393 tiles of GPT-2's
-// vocabulary at 64 token rows fit 3 CTAs per SM with 2 stages, 2 with 3).
-int plan_dl_stages(int dev, int num_sms, int kb, int splits, int rows, int n_tiles) {
-  int st = dl_stages(kb, splits);
-  if (splits == 1 && st == 3) {
-    const int bi = dl_bp(rows) / 8 - 1;
-    const long long cap3 = static_cast<long long>(g_dl_max_blocks[dev][bi][2]) * num_sms;
-    const long long cap2 = static_cast<long long>(g_dl_max_blocks[dev][bi][1]) * num_sms;
-    if (n_tiles > cap3 && n_tiles <= cap2) st = 2;
-  }
-  return st;
-}
 
 // Split-K factor (= cluster size): the largest power of two <= 16 and <= the k-block count
 // that keeps the grid within 2/3 of the SMs and all clusters resident in one wave.  (Fewer,
@@ -838,7 +814,7 @@ int dec_linear(gpt_model* m, const bf16* A, const void* W, int M, int N, int K, 
   e.N = N;
   e.T = 1;
   e.err = m->d_err;
-  CK(launch_dl(epi, tw, tx, kb, splits, plan_dl_stages(m->dev, m->num_sms, kb, splits, M, n_tiles), n_tiles, e, true,
+  CK(launch_dl(epi, tw, tx, kb, splits, dl_stages(kb, splits), n_tiles, e, true,
                m->stream));
   ++m->launches;
   return GPT_OK;
@@ -1725,7 +1701,7 @@ int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, floa
   e.x = out;
   e.ldx = N;
   e.err = c->err;
-  CK(launch_dl(EPI_F32, tw, tx, kb, splits, plan_dl_stages(dev, num_sms, kb, splits, M, n_tiles), n_tiles, e, false,
+  CK(launch_dl(EPI_F32, tw, tx, kb, splits, dl_stages(kb, splits), n_tiles, e, false,
                static_cast<cudaStream_t>(stream)));
   return GPT_OK;
 }
@@ -1767,7 +1743,7 @@ int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const flo
   e.ln_g = gamma;
   e.ln_b = beta;
   // the operand is built in shared memory: the activation map is never loaded (W's map stands in)
-  CK(launch_dl(EPI_F32, tw, tw, kb, splits, plan_dl_stages(dev, num_sms, kb, splits, M, n_tiles), n_tiles, e, false,
+  CK(launch_dl(EPI_F32, tw, tw, kb, splits, dl_stages(kb, splits), n_tiles, e, false,
                static_cast<cudaStream_t>(stream)));
   return GPT_OK;
 }
