@@ -217,32 +217,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Make this thread's generic-proxy shared-memory writes visible to later async-proxy (TMA /
-// bulk copy) reads.
+// Make this thread's generic-proxy shared-memory writes visible to later async-proxy reads
+// (the tensor core's operand fetch).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from this CTA's shared memory to the
-// shared memory of a CTA of the cluster (dst and its mbarrier as shared::cluster addresses);
-// the bytes are counted on that mbarrier's transaction count when they land.
-__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "r"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk copy of this thread has finished reading its source.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // Shared-memory matrix descriptor for a K-major bf16 tile written by TMA with 128-byte
 // swizzle: rows of 128 B (64 elements), 8-row groups 1024 B apart, tile base 1024-aligned.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
