@@ -423,6 +423,10 @@ def run_ours(args, rank, world, local_rank):
         G.gpt_attention_decode(q, kc, vc, pos[i:i + 1], 1, y, ylo)
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(N - 1)]
+    # A spin kernel at the head of the stream holds the GPU while the host enqueues every
+    # launch with its two events, so that each event pair brackets exactly one kernel (from
+    # the end of the previous one) and never host time between launches.
+    torch.cuda._sleep(int(2e8))
     for i, (a, b) in enumerate(evs):
         a.record()
         G.gpt_attention_decode(q, kc, vc, pos[i:i + 1], 1, y, ylo)
