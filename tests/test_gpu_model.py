@@ -354,6 +354,42 @@ def test_paged_cache_gives_the_contiguous_results(dtype, page):
     assert flat.sync_status() == G.GPT_OK and paged.sync_status() == G.GPT_OK
 
 
+def test_two_chain_decode_with_paged_cache():
+    """From 32 sequences up a decode step runs as two chains of half the batch on two streams,
+    the second addressing its sequences through an offset into the cache (contiguous) or into
+    the block tables (paged).  Paged and contiguous caches give bit-identical logits, across
+    page boundaries, through generate and a ragged batch; rows of both chains match the
+    oracle."""
+    shape = syn.ModelShape(2, 2, 128, 256, 300, True, "bf16")
+    sd = syn.make_weights(shape, seed=41, bias_std=0.05, random_gamma=True)
+    cfg, w = oracle_model(shape, sd)
+    B = 40
+    flat = make_gpu_model(shape, sd, B)
+    paged = make_gpu_model(shape, sd, B, page_size=64, n_pages=B * 4)
+    prompt = syn.make_tokens(B, 70, 300, seed=3)
+    pd = torch.from_numpy(prompt).cuda()
+    assert torch.equal(flat.prefill(pd), paged.prefill(pd))
+    seqs = prompt.copy()
+    for step in range(70):  # crosses the page boundary at position 128
+        tok = syn.make_tokens(B, 1, 300, seed=300 + step)[:, 0].copy()
+        seqs = np.concatenate([seqs, tok[:, None]], axis=1)
+        a = flat.decode_step(torch.from_numpy(tok).cuda())
+        assert torch.equal(a, paged.decode_step(torch.from_numpy(tok).cuda())), step
+    got = a.cpu().numpy()
+    for r in (0, 19, 20, 39):  # first and last rows of each chain
+        ref = og.forward(cfg, w, seqs[r:r + 1])[0][0]
+        assert np.max(np.abs(got[r] - ref)) < BF16_TOL, r
+    p40 = pd[:, :40].contiguous()
+    assert torch.equal(flat.generate(p40, 100, temperature=0.8, top_k=30, seed=5),
+                       paged.generate(p40, 100, temperature=0.8, top_k=30, seed=5))
+    lens = [1 + (7 * b) % 70 for b in range(B)]
+    assert torch.equal(flat.prefill_ragged(pd, lens), paged.prefill_ragged(pd, lens))
+    for step in range(5):
+        tok = torch.from_numpy(syn.make_tokens(B, 1, 300, seed=400 + step)[:, 0].copy()).cuda()
+        assert torch.equal(flat.decode_step(tok), paged.decode_step(tok))
+    assert flat.sync_status() == G.GPT_OK and paged.sync_status() == G.GPT_OK
+
+
 def test_paged_cache_reports_an_exhausted_pool():
     shape = syn.ModelShape(1, 2, 128, 256, 100, False, "bf16")
     sd = syn.make_weights(shape, seed=4)
