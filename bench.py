@@ -80,9 +80,9 @@ def decode_step_bytes(shape, B, P, steps):
 
 
 def secondary_workload(G, syn, name, dev, seed, hbm):
-    """Prefill and decode rates of another configuration of the survey's measurement table
-    (one gpt_generate per run: a prefill of the prompt, then the workload's decode steps;
-    median of 3 runs after one warm-up), with the decode step's fraction of the HBM roofline."""
+    """Prefill and decode rates of another workload configuration (one gpt_generate per run:
+    a prefill of the prompt, then the workload's decode steps; median of 3 runs after one
+    warm-up), with the decode step's fraction of the HBM roofline."""
     import torch
 
     wl = syn.WORKLOADS[name]

@@ -26,7 +26,7 @@ Pages restated (title, site, section):
   [guide]   "LLM研究框架选择指南：从nanoGPT到nanochat的实战分析" (intelliparadigm.com),
             §2.1 Block: x = x + attn(ln_1(x)); x = x + mlp(ln_2(x)), MLP with nn.GELU().
 
-Readings where the pages leave a step open (each also listed in the design doc):
+Readings where the pages leave a step open:
   * GELU is the exact erf form (nn.GELU()'s default; no approximation is named).
   * LayerNorm variance is the biased one (F.layer_norm's definition).
   * c_attn's output splits into q | k | v blocks of n_embd columns; head h owns
