@@ -148,6 +148,9 @@ int gpt_extend(gpt_model_t* model, const int32_t* tokens, int32_t T, float* logi
 /* One KV-cached step: append token tokens[b] (dev, int32, B = the prefill's batch) at
  * position = current cache length, and write that position's logits (dev, fp32,
  * B x vocab_size).  The cache length grows by one.
+ * From 32 sequences up (bf16) the step runs as two chains of half the batch, the second on a
+ * library-owned stream that waits on the model's stream and is joined back into it before
+ * the call returns: the work is still ordered on the model's stream as for any other call.
  * Errors: GPT_ESTATE (no prefill yet), GPT_ECONTEXT (cache full), GPT_EINVAL, GPT_ECUDA. */
 int gpt_decode_step(gpt_model_t* model, const int32_t* tokens, float* logits);
 
