@@ -173,11 +173,12 @@ class ClockSampler:
 
 
 def blas_threads() -> int:
-    """Threads numpy's BLAS runs with (all usable host cores unless capped by the environment)."""
+    """Threads numpy's BLAS runs with (all usable host cores unless capped by the environment
+    or a threadpool limit); other thread pools in the process (torch's OpenMP) do not count."""
     try:
         from threadpoolctl import threadpool_info
 
-        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"] or [1])
     except ImportError:
         for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
             if os.environ.get(var, "").isdigit():
@@ -208,6 +209,32 @@ def oracle_sample(n_rows: int, n_decode: int):
     t2 = time.perf_counter()
     threads = blas_threads()
     return n_rows * wl.prompt / (t1 - t0), n_rows * n_decode / (t2 - t1), threads, t2 - t0
+
+
+def oracle_single_thread(n_rows: int = 1, n_decode: int = 2):
+    """The oracle's decode rate with numpy's BLAS held to one thread (a smaller sample: one
+    sequence's 512-token prefill and two decode steps).  None where the thread pool cannot be
+    limited."""
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        return None
+    # load every BLAS the oracle uses (numpy's and scipy's) before the limit is taken
+    import oracle.gpt  # noqa: F401
+    import oracle.sampler  # noqa: F401
+
+    with threadpool_limits(limits=1, user_api="blas"):
+        _, d, threads, secs = oracle_sample(n_rows, n_decode)
+    if threads != 1:
+        return None
+    return {"value": d, "unit": "tok/s", "cores": 1, "seconds": secs,
+            "sample": f"{n_rows} sequence: {syn_prompt_len()}-token prefill + {n_decode} decode steps, one thread"}
+
+
+def syn_prompt_len() -> int:
+    from kv_cached_generation_gpt_b300 import synthetic as syn
+
+    return syn.WORKLOADS[WORKLOAD].prompt
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -446,6 +473,10 @@ def run_ours(args, rank, world, local_rank):
         cpu = {"value": d, "unit": "tok/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} of {B} sequences: {P}-token prefill + {dec} decode steps with the workload's "
                          f"sampling, fp64 numpy on the host"}
+        try:
+            cpu["single_thread"] = oracle_single_thread()
+        except Exception as ex:  # a reported extra: never let it cost the bench line
+            cpu["single_thread"] = {"error": str(ex)[:200]}
 
     if rank != 0:
         return

@@ -70,3 +70,17 @@ def test_decode_attention_bytes_per_launch():
     b = _bench()
     # B = 64, 12 heads of 64, 768 keys: K and V rows read once, q read, y hi and lo written
     assert b.decode_attn_bytes(64, 12, 64, 768) == 2 * 64 * 12 * 768 * 64 * 2 + 64 * 12 * 64 * 2 * 3
+
+
+def test_cpu_baseline_thread_count_follows_the_blas_limit():
+    """cpu_baseline reports the threads numpy's BLAS ran with: a one-thread limit on the BLAS
+    pools (numpy's and scipy's, loaded with the oracle) reads back as 1, whatever other thread
+    pools (torch's OpenMP) hold."""
+    threadpoolctl = pytest.importorskip("threadpoolctl")
+    import oracle.gpt  # noqa: F401
+    import oracle.sampler  # noqa: F401
+
+    b = _bench()
+    with threadpoolctl.threadpool_limits(limits=1, user_api="blas"):
+        assert b.blas_threads() == 1
+    assert b.blas_threads() >= 1
