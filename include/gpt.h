@@ -240,8 +240,8 @@ int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, floa
  * decode step of up to 8 sequences runs ln_1 + c_attn, ln_2 + c_fc and ln_f + lm_head
  * ("nanoGPT 架构分析", §4.1: pre-LN blocks).  Every CTA takes the whole rows' statistics and
  * normalises its own K-slice.  x (dev, fp32): M rows of K, row r at x + r * x_stride
- * (x_stride % 4 == 0, 16-byte aligned); 1 <= M <= 8; K <= 2048; gamma (dev, fp32, K); beta
- * (dev, fp32, K) or NULL; W, bias, splits as in gpt_linear_decode_bf16. */
+ * (x_stride % 4 == 0, 16-byte aligned); 1 <= M <= 8; K <= 2048; gamma (dev, fp32, K) and beta
+ * (dev, fp32, K, or NULL) 16-byte aligned; W, bias, splits as in gpt_linear_decode_bf16. */
 int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const float* gamma, const float* beta,
                                      const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
                                      int32_t splits, void* stream);
@@ -249,7 +249,9 @@ int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const flo
 /* y (dev, dtype, rows x C) = LayerNorm(x) with eps 1e-5 and biased variance.
  * x (dev, fp32) row r at x + r * x_stride; gamma (dev, fp32, C); beta (dev, fp32, C) or NULL.
  * y_lo (dev, bf16) or NULL: receives y - bf16(y) (only with dtype == GPT_DTYPE_BF16).
- * C % 64 == 0 and C <= 2048. */
+ * C % 64 == 0 and C <= 2048.  The kernel moves column pairs: x_stride even, x, gamma and
+ * beta 8-byte aligned, y 4-byte (bf16) or 8-byte (fp32) aligned, y_lo 4-byte aligned;
+ * anything else is GPT_EINVAL. */
 int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const float* beta, int32_t rows, int32_t C,
                   int32_t dtype, void* y, void* y_lo, void* stream);
 

@@ -1706,12 +1706,18 @@ int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, floa
   return GPT_OK;
 }
 
+namespace {
+bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
+}  // namespace
+
 int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const float* gamma, const float* beta,
                                      const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
                                      int32_t splits, void* stream) {
   if (!x || !gamma || !W || !out || M < 1 || M > DL_LN_MAX_ROWS || N < 1 || K < 64 || K % 64 != 0 ||
       K > 64 * LN_MAX_PAIRS || splits < 0 || x_stride < K || x_stride % 4 != 0)
     return GPT_EINVAL;
+  // 16-byte loads of x, gamma and beta build the operand
+  if (!aligned(x, 16) || !aligned(gamma, 16) || (beta && !aligned(beta, 16))) return GPT_EINVAL;
   const int kb = K / TC_BK;
   if (splits > 0 && ((splits & (splits - 1)) != 0 || splits > DL_MAX_SPLITS || splits > kb)) return GPT_EINVAL;
   int dev = 0;
@@ -1753,6 +1759,10 @@ int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const fl
   if (!x || !gamma || !y || rows < 1 || C < 64 || C % 64 != 0 || C > 64 * LN_MAX_PAIRS || x_stride < C) return GPT_EINVAL;
   if (dtype != GPT_DTYPE_BF16 && dtype != GPT_DTYPE_F32) return GPT_EINVAL;
   if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;
+  // the kernel moves column pairs: 8-byte loads of x, gamma and beta, pair stores of y
+  if (x_stride % 2 != 0 || !aligned(x, 8) || !aligned(gamma, 8) || (beta && !aligned(beta, 8)) ||
+      !aligned(y, dtype == GPT_DTYPE_BF16 ? 4 : 8) || (y_lo && !aligned(y_lo, 4)))
+    return GPT_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == GPT_DTYPE_BF16)
     CK(launch_ln<bf16>(rows, C, x_stride, x, gamma, beta, static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, st,

@@ -70,6 +70,13 @@ def test_stand_alone_ops_reject_bad_arguments_on_the_host():
     assert lib.gpt_linear_bf16(p, p, None, p, 4, 64, 128, 1, 256, 1, None) == G.GPT_EINVAL  # hilo + 256
     assert lib.gpt_linear_bf16(p, p, None, p, 4, 65, 128, 0, 0, 2, None) == G.GPT_EINVAL  # split with N % 16
     assert lib.gpt_layernorm(p, 96, p, None, 4, 96, 1, p, None, None) == G.GPT_EINVAL  # C % 64
+    assert lib.gpt_layernorm(p, 129, p, None, 4, 128, 1, p, None, None) == G.GPT_EINVAL  # odd row stride
+    assert lib.gpt_layernorm(ctypes.c_void_p(20), 128, p, None, 4, 128, 1, p, None, None) == G.GPT_EINVAL  # x % 8
+    ln_lin = lib.gpt_layernorm_linear_decode_bf16
+    assert ln_lin(p, 768, p, None, p, None, p, 9, 64, 768, 0, None) == G.GPT_EINVAL  # more than 8 rows
+    assert ln_lin(ctypes.c_void_p(24), 768, p, None, p, None, p, 4, 64, 768, 0, None) == G.GPT_EINVAL  # x % 16
+    assert ln_lin(p, 768, ctypes.c_void_p(40), None, p, None, p, 4, 64, 768, 0, None) == G.GPT_EINVAL  # gamma
+    assert ln_lin(p, 770, p, None, p, None, p, 4, 64, 768, 0, None) == G.GPT_EINVAL  # stride % 4
     assert lib.gpt_attention_prefill(p, p, p, 1, 1, 2, 64, 8, 4, 0, p, None) == G.GPT_EINVAL  # T > block
     assert lib.gpt_attention_prefill(p, p, p, 1, 1, 2, 32, 4, 8, 0, p, None) == G.GPT_EINVAL  # bf16 needs hs 64
     assert lib.gpt_sample(p, 1, 60000, ctypes.c_float(1.0), 0, 0, 0, p, None, None, None) == G.GPT_EINVAL
