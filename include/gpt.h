@@ -24,6 +24,10 @@
  *     pipeline wait that timed out) are recorded in a device error word and reported by
  *     gpt_sync_status() / gpt_op_status(); kernels never trap.
  *   - Head size n_embd / n_head: 64 (every GPT-2 shape), or 32 for fp32 models.
+ *   - The stand-alone operations check pointer alignment on the host (GPT_EINVAL otherwise):
+ *     16 bytes for the operands their kernels move in 16-byte vectors (Linear outputs,
+ *     attention q / k / v, the fused LayerNorm operand), as stated per entry point.
+ *     Allocations from cudaMalloc or torch always qualify.
  */
 #ifndef KVGPT_GPT_H
 #define KVGPT_GPT_H
@@ -218,7 +222,8 @@ const char* gpt_last_error_detail(void);
  * (N % 128 == 0) tile per SM, the persistent kernel (one CTA per SM walking the tiles, two TMEM
  * accumulators so the epilogue of one tile overlaps the next tile's MMAs).
  * splits: split-K count >= 1 (needs N % 16 == 0 when > 1); partial sums go to library-owned
- * scratch and are added in split order, so results do not depend on CTA timing. */
+ * scratch and are added in split order, so results do not depend on CTA timing.
+ * out 16-byte aligned. */
 int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
                     int32_t K, int32_t hilo, int32_t block_n, int32_t splits, void* stream);
 
@@ -230,7 +235,7 @@ int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out,
  * over the CTAs of one thread-block cluster and reduced in split order through distributed
  * shared memory (deterministic, no scratch memory).  splits: 0 = chosen by the library, else
  * a power of two <= 16 and <= K/64 (16 needs 16-CTA clusters: GPT_EUNSUPPORTED where the
- * device cannot schedule them). */
+ * device cannot schedule them).  out 16-byte aligned. */
 int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
                            int32_t K, int32_t splits, void* stream);
 
@@ -259,7 +264,8 @@ int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const fl
  * q (dev, dtype): B x n_head x T x hs.  k_cache, v_cache (dev, dtype): B x n_head x block x
  * hs, holding keys for positions 0 .. pos0+T-1.  Query t sits at position pos0 + t and sees
  * keys 0 .. pos0+t.  y (dev, dtype): (B*T) x (hs*n_head), row b*T + t, column h*hs + d.
- * bf16 runs on tensor cores (mma.sync), fp32 exactly in fp32 (pos0 + T <= 12288). */
+ * bf16 runs on tensor cores (mma.sync), fp32 exactly in fp32 (pos0 + T <= 12288).
+ * q, k_cache and v_cache 16-byte aligned. */
 int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
                           int32_t n_head, int32_t head_size, int32_t T, int32_t block, int32_t pos0, void* y,
                           void* stream);
@@ -268,7 +274,8 @@ int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cach
  * head_size 32 or 64.  q (dev, dtype): B x n_head x hs; caches as above; pos0_dev (dev,
  * int32): cache length before the new token.  splits >= 1: the keys are split across that
  * many CTAs per (b, h) and merged by log-sum-exp in split order (library-owned scratch).
- * y (dev, dtype): B x (hs*n_head); y_lo (dev, bf16) or NULL receives y - bf16(y). */
+ * y (dev, dtype): B x (hs*n_head); y_lo (dev, bf16) or NULL receives y - bf16(y).
+ * q, k_cache and v_cache 16-byte aligned. */
 int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
                          int32_t n_head, int32_t head_size, int32_t block, const int32_t* pos0_dev, int32_t splits,
                          void* y, void* y_lo, void* stream);

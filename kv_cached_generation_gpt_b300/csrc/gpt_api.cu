@@ -1305,6 +1305,12 @@ int create_impl(const gpt_config_t* cfg, const gpt_weights_t* w, void* stream, g
 
 // ====================================================================== C ABI
 
+namespace {
+// Pointer alignment the stand-alone entry points check before any launch (their kernels use
+// vector loads and stores of that width).
+bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
+}  // namespace
+
 extern "C" {
 
 const char* gpt_strerror(int code) {
@@ -1618,6 +1624,7 @@ int gpt_sync_status(gpt_model_t* m) {
 int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
                     int32_t hilo, int32_t block_n, int32_t splits, void* stream) {
   if (!A || !W || !out || M < 1 || N < 1 || K < 64 || K % 64 != 0 || splits < 1) return GPT_EINVAL;
+  if (!aligned(out, 16)) return GPT_EINVAL;  // 16-byte stores of output rows
   if (block_n != 0 && block_n != 64 && block_n != 128 && block_n != 256) return GPT_EINVAL;
   if (hilo && block_n == 256) return GPT_EINVAL;
   if (splits > 1 && N % 16 != 0) return GPT_EINVAL;
@@ -1674,6 +1681,7 @@ int gpt_linear_bf16(const void* A, const void* W, const float* bias, float* out,
 int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, float* out, int32_t M, int32_t N,
                            int32_t K, int32_t splits, void* stream) {
   if (!A || !W || !out || M < 1 || M > DL_MAX_ROWS || N < 1 || K < 64 || K % 64 != 0 || splits < 0) return GPT_EINVAL;
+  if (!aligned(out, 16)) return GPT_EINVAL;  // 16-byte stores of output rows
   const int kb = K / TC_BK;
   if (splits > 0 && ((splits & (splits - 1)) != 0 || splits > DL_MAX_SPLITS || splits > kb)) return GPT_EINVAL;
   int dev = 0;
@@ -1706,18 +1714,14 @@ int gpt_linear_decode_bf16(const void* A, const void* W, const float* bias, floa
   return GPT_OK;
 }
 
-namespace {
-bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
-}  // namespace
-
 int gpt_layernorm_linear_decode_bf16(const float* x, int64_t x_stride, const float* gamma, const float* beta,
                                      const void* W, const float* bias, float* out, int32_t M, int32_t N, int32_t K,
                                      int32_t splits, void* stream) {
   if (!x || !gamma || !W || !out || M < 1 || M > DL_LN_MAX_ROWS || N < 1 || K < 64 || K % 64 != 0 ||
       K > 64 * LN_MAX_PAIRS || splits < 0 || x_stride < K || x_stride % 4 != 0)
     return GPT_EINVAL;
-  // 16-byte loads of x, gamma and beta build the operand
-  if (!aligned(x, 16) || !aligned(gamma, 16) || (beta && !aligned(beta, 16))) return GPT_EINVAL;
+  // 16-byte loads of x, gamma and beta build the operand; 16-byte stores of output rows
+  if (!aligned(x, 16) || !aligned(gamma, 16) || (beta && !aligned(beta, 16)) || !aligned(out, 16)) return GPT_EINVAL;
   const int kb = K / TC_BK;
   if (splits > 0 && ((splits & (splits - 1)) != 0 || splits > DL_MAX_SPLITS || splits > kb)) return GPT_EINVAL;
   int dev = 0;
@@ -1778,6 +1782,7 @@ int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cach
                           void* stream) {
   if (!q || !k_cache || !v_cache || !y || B < 1 || n_head < 1 || T < 1 || pos0 < 0 || pos0 + T > block)
     return GPT_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return GPT_EINVAL;  // 16-byte row loads
   if (head_size != 64 && !(head_size == 32 && dtype == GPT_DTYPE_F32)) return GPT_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int C = head_size * n_head;
@@ -1807,6 +1812,7 @@ int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache
   if (!q || !k_cache || !v_cache || !y || !pos0_dev || B < 1 || n_head < 1 || block < 1 || splits < 1 ||
       splits > 1024)
     return GPT_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return GPT_EINVAL;  // 16-byte row loads
   if (head_size != 64 && head_size != 32) return GPT_EINVAL;
   if (dtype != GPT_DTYPE_BF16 && dtype != GPT_DTYPE_F32) return GPT_EINVAL;
   if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;
@@ -1921,6 +1927,7 @@ int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void*
   if (!q || !k_cache || !v_cache || !y || !pos0_dev || B < 1 || n_head < 1 || block < 1 || splits < 1 ||
       splits > 1024)
     return GPT_EINVAL;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return GPT_EINVAL;  // 16-byte row loads
   if (head_size != 64 && head_size != 32) return GPT_EINVAL;
   if (dtype != GPT_DTYPE_BF16 && dtype != GPT_DTYPE_F32) return GPT_EINVAL;
   if (y_lo && dtype != GPT_DTYPE_BF16) return GPT_EINVAL;

@@ -72,6 +72,11 @@ def test_stand_alone_ops_reject_bad_arguments_on_the_host():
     assert lib.gpt_layernorm(p, 96, p, None, 4, 96, 1, p, None, None) == G.GPT_EINVAL  # C % 64
     assert lib.gpt_layernorm(p, 129, p, None, 4, 128, 1, p, None, None) == G.GPT_EINVAL  # odd row stride
     assert lib.gpt_layernorm(ctypes.c_void_p(20), 128, p, None, 4, 128, 1, p, None, None) == G.GPT_EINVAL  # x % 8
+    q = ctypes.c_void_p(24)  # 8-byte but not 16-byte aligned
+    assert lib.gpt_linear_bf16(p, p, None, q, 4, 64, 128, 0, 0, 1, None) == G.GPT_EINVAL  # out % 16
+    assert lib.gpt_linear_decode_bf16(p, p, None, q, 4, 64, 128, 0, None) == G.GPT_EINVAL  # out % 16
+    assert lib.gpt_attention_prefill(q, p, p, 1, 1, 2, 64, 4, 8, 0, p, None) == G.GPT_EINVAL  # q % 16
+    assert lib.gpt_attention_decode(p, q, p, 1, 1, 2, 64, 8, p, 1, p, None, None) == G.GPT_EINVAL  # k % 16
     ln_lin = lib.gpt_layernorm_linear_decode_bf16
     assert ln_lin(p, 768, p, None, p, None, p, 9, 64, 768, 0, None) == G.GPT_EINVAL  # more than 8 rows
     assert ln_lin(ctypes.c_void_p(24), 768, p, None, p, None, p, 4, 64, 768, 0, None) == G.GPT_EINVAL  # x % 16
