@@ -211,30 +211,72 @@ def oracle_sample(n_rows: int, n_decode: int):
     return n_rows * wl.prompt / (t1 - t0), n_rows * n_decode / (t2 - t1), threads, t2 - t0
 
 
-def oracle_single_thread(n_rows: int = 1, n_decode: int = 2):
-    """The oracle's decode rate with numpy's BLAS held to one thread (a smaller sample: one
-    sequence's 512-token prefill and two decode steps).  None where the thread pool cannot be
-    limited."""
-    try:
-        from threadpoolctl import threadpool_limits
-    except ImportError:
-        return None
-    # load every BLAS the oracle uses (numpy's and scipy's) before the limit is taken
-    import oracle.gpt  # noqa: F401
-    import oracle.sampler  # noqa: F401
+ONE_THREAD_ENV = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
 
-    with threadpool_limits(limits=1, user_api="blas"):
-        _, d, threads, secs = oracle_sample(n_rows, n_decode)
-    if threads != 1:
-        return None
-    return {"value": d, "unit": "tok/s", "cores": 1, "seconds": secs,
-            "sample": f"{n_rows} sequence: {syn_prompt_len()}-token prefill + {n_decode} decode steps, one thread"}
+
+def oracle_single_thread(n_rows: int = 1, n_decode: int = 2):
+    """The oracle's decode rate with numpy's BLAS held to one thread: a fresh interpreter (this
+    file's --oracle-leg mode) started with the BLAS thread variables set to 1, on a smaller sample
+    (one sequence's 512-token prefill and two decode steps)."""
+    env = dict(os.environ, **ONE_THREAD_ENV)
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", f"{n_rows},{n_decode}"],
+                         env=env, capture_output=True, text=True, timeout=600)
+    if res.returncode != 0:
+        raise RuntimeError(res.stderr[-300:])
+    pre, dec, threads, secs = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": dec, "unit": "tok/s", "cores": threads, "seconds": secs, "prefill_tok_s": pre,
+            "sample": f"{n_rows} sequence: {syn_prompt_len()}-token prefill + {n_decode} decode steps, "
+                      f"BLAS held to one thread"}
 
 
 def syn_prompt_len() -> int:
     from kv_cached_generation_gpt_b300 import synthetic as syn
 
     return syn.WORKLOADS[WORKLOAD].prompt
+
+
+def host_facts() -> dict:
+    """Host CPU count and model (from /proc/cpuinfo)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"host_cpus": os.cpu_count(), "usable_cpus": len(os.sched_getaffinity(0)), "cpu_model": model}
+
+
+def oracle_configs(max_b1_steps: int = 48):
+    """The oracle on the other workload configurations: the tiny (fp32, greedy) and char-level
+    (temperature 0.8, top-k 200) ones in full, GPT-2 124M at batch 1 on a bounded sample (its
+    128-token prefill and the first max_b1_steps of its 896 decode steps)."""
+    from kv_cached_generation_gpt_b300 import synthetic as syn
+    from oracle import gpt as og
+    from oracle import sampler as osm
+
+    rows = []
+    for name, n_dec in (("tiny_b1_p16_d32", None), ("char_b1_p1_d255", None), (B1_WORKLOAD, max_b1_steps)):
+        wl = syn.WORKLOADS[name]
+        shape = wl.model
+        n = wl.decode_steps if n_dec is None else min(n_dec, wl.decode_steps)
+        sd = syn.storage_values(shape, syn.make_weights(shape, bias_std=wl.bias_std))
+        cfg = og.Config(shape.n_layer, shape.n_head, shape.n_embd, shape.block_size, shape.vocab_size, shape.bias)
+        w = og.weights_from_state_dict(cfg, sd)
+        prompt = syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)
+        t0 = time.perf_counter()
+        logits, cache = og.prefill(cfg, w, prompt)
+        t1 = time.perf_counter()
+        for j in range(n):
+            tok = osm.sample(logits.astype(np.float32), wl.temperature, wl.top_k, 1, j)
+            logits, cache = og.decode(cfg, w, cache, tok)
+        t2 = time.perf_counter()
+        rows.append({"workload": name, "prefill_tok_s": wl.batch * wl.prompt / (t1 - t0),
+                     "decode_tok_s": wl.batch * n / (t2 - t1), "decode_steps_timed": n,
+                     "full": n == wl.decode_steps})
+    return rows
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -263,7 +305,8 @@ def run_reference(args, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded random-init GPT-2 124M weights rounded to bf16, uniform token ids)",
         "config": workload_config(wl),
-        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         **host_facts()},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -473,10 +516,15 @@ def run_ours(args, rank, world, local_rank):
         cpu = {"value": d, "unit": "tok/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} of {B} sequences: {P}-token prefill + {dec} decode steps with the workload's "
                          f"sampling, fp64 numpy on the host"}
+        cpu.update(host_facts())
         try:
             cpu["single_thread"] = oracle_single_thread()
         except Exception as ex:  # a reported extra: never let it cost the bench line
             cpu["single_thread"] = {"error": str(ex)[:200]}
+        try:
+            cpu["configs"] = oracle_configs()
+        except Exception as ex:
+            cpu["configs"] = {"error": str(ex)[:200]}
 
     if rank != 0:
         return
@@ -528,7 +576,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-leg", default=None, help=argparse.SUPPRESS)  # "rows,decode": CPU only
     args = ap.parse_args()
+    if args.oracle_leg:
+        rows, dec = (int(v) for v in args.oracle_leg.split(","))
+        print(json.dumps(list(oracle_sample(rows, dec))), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

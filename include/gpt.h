@@ -97,7 +97,9 @@ typedef struct gpt_model gpt_model_t;
 
 /* ------------------------------------------------------------------ model */
 
-/* Validate `cfg`, copy the weights into library-owned device buffers, and allocate the KV
+/* GPT(config) of the pages ("极速上手nanoGPT", §GPTConfig类: block_size, vocab_size, n_layer,
+ * n_head, n_embd, bias; "nanoGPT 架构分析", §4.1: the modules and the wte / lm_head tying).
+ * Validate `cfg`, copy the weights into library-owned device buffers, and allocate the KV
  * cache (n_layer x 2 x max_batch x n_head x block_size x 64 elements) and all scratch.
  * Keeps no caller pointer after it returns.  Synchronises `stream` once (weight copy).
  * Errors: GPT_EINVAL (bad cfg / weights), GPT_EUNSUPPORTED (not sm_103), GPT_ENOMEM,
@@ -115,8 +117,9 @@ int gpt_create(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stre
 int gpt_create_paged(const gpt_config_t* cfg, const gpt_weights_t* weights, void* stream, int32_t page_size,
                      int32_t n_pages, gpt_model_t** out);
 
-/* Release everything gpt_create allocated (synchronises the model's stream first).
- * NULL is a no-op. */
+/* Release everything gpt_create allocated -- the weights, the KV cache the sketch of
+ * "原生 nanoGPT 模型服务首选", §"一个值得做的改进" keeps between steps, and all scratch
+ * (synchronises the model's stream first).  NULL is a no-op. */
 void gpt_destroy(gpt_model_t* model);
 
 /* Prefill from an empty cache: run the prompt tokens (dev, int32, B x T row-major) through
@@ -149,9 +152,12 @@ int gpt_prefill_ragged(gpt_model_t* model, const int32_t* tokens, const int32_t*
  * Errors: GPT_ESTATE (no prefill yet), GPT_ECONTEXT (cache length + T > block_size), GPT_EINVAL. */
 int gpt_extend(gpt_model_t* model, const int32_t* tokens, int32_t T, float* logits);
 
-/* One KV-cached step: append token tokens[b] (dev, int32, B = the prefill's batch) at
- * position = current cache length, and write that position's logits (dev, fp32,
- * B x vocab_size).  The cache length grows by one.
+/* One KV-cached step, the forward(x, past_kv) of "原生 nanoGPT 模型服务首选",
+ * §"一个值得做的改进": only the new token is fed, its K/V are appended to the cache and its
+ * query attends to every cached key (no mask is needed for a single new token).
+ * Append token tokens[b] (dev, int32, B = the prefill's batch) at position = current cache
+ * length, and write that position's logits (dev, fp32, B x vocab_size).  The cache length
+ * grows by one.
  * From 32 sequences up (bf16) the step runs as two chains of half the batch, the second on a
  * library-owned stream that waits on the model's stream and is joined back into it before
  * the call returns: the work is still ordered on the model's stream as for any other call.
@@ -293,6 +299,24 @@ int gpt_sample(const float* logits, int32_t B, int32_t V, float temperature, int
  * word (codes as gpt_sync_status). */
 int gpt_op_status(void);
 
+/* ------------------------------------------------------------------ failure-detection hooks
+ * Test hooks for the library's own error paths ("nanoGPT 架构分析", §9 总结与评价, 可改进之处:
+ * the reference code has no error handling; these let a test reach each path without a GPU
+ * fault). */
+
+/* Launch one CTA that waits on a shared-memory mbarrier with the library's bounded wait, for at
+ * most limit_us microseconds (1 .. 1,000,000).  arrive = 1: the CTA arrives first and the wait
+ * succeeds at once; arrive = 0: nothing arrives, the wait runs out, the kernel records the
+ * timeout in the stand-alone operations' error word and returns (gpt_op_status() then gives
+ * GPT_ETIMEOUT).  The context stays usable.  Errors: GPT_EINVAL for limit_us out of range. */
+int gpt_debug_bounded_wait(int32_t limit_us, int32_t arrive, void* stream);
+
+/* Make the k-th next device allocation a model makes (gpt_create / gpt_create_paged, counted
+ * across threads, process-wide) fail as if the device were out of memory; k = 0 turns the
+ * injection off.  The create call then returns GPT_ENOMEM, leaves *out NULL and frees what it
+ * had allocated.  Errors: GPT_EINVAL for k < 0. */
+int gpt_debug_fail_allocation(int32_t k);
+
 /* gpt_attention_decode for callers that cannot allocate device memory.  The pages have no
  * counterpart: this is a deployment variant, not a step of the method.
  *
@@ -307,10 +331,13 @@ int gpt_op_status(void);
  * error bits the kernel finds (a position at or beyond block) are OR-ed into *err_dev, in the
  * bit layout gpt_sync_status decodes (4 = position); with NULL they are dropped.
  * Limits: B * n_head <= 16384, and when splits > 1, B * n_head * splits * (head_size + 2) * 4
- * bytes must fit in 4 MiB minus 64 KiB; larger requests return GPT_ETOOBIG before anything is
+ * bytes must not exceed 4,128,512 (the 4 MiB array minus a 256-byte error-word header and
+ * 16384 four-byte merge tickets); larger requests return GPT_ETOOBIG before anything is
  * enqueued (gpt_last_error_detail() gives the sizes).
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  Every call shares the
+ * that device current and keeps it for the life of the process; make that first call before
+ * any stream capture (a first call on a capturing stream returns GPT_EUNSUPPORTED), and make
+ * no call after a cudaDeviceReset, which invalidates the kept address.  Every call shares the
  * array, which keeps the previous call's contents: the call clears the tickets it uses (an
  * asynchronous memset on `stream`), and calls whose kernels overlap on the same GPU (for
  * example on two streams) race on the array: the caller must serialise them. */

@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <tuple>
@@ -44,6 +45,18 @@ struct PagedRequest {
   int page_size = 0, n_pages = 0;
 };
 thread_local PagedRequest g_paged_request;
+
+// Failure injection for tests (gpt_debug_fail_allocation): when positive, the allocation that
+// brings it to zero fails as if the device were out of memory.
+std::atomic<int> g_fail_alloc_countdown{0};
+
+bool fail_this_allocation() {
+  int c = g_fail_alloc_countdown.load();
+  while (c > 0) {
+    if (g_fail_alloc_countdown.compare_exchange_weak(c, c - 1)) return c == 1;
+  }
+  return false;
+}
 
 int cuda_fail(cudaError_t e, const char* what) {
   g_detail = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
@@ -637,7 +650,7 @@ struct gpt_model {
   template <typename T>
   T* alloc(size_t count, int* rc) {
     void* p = nullptr;
-    cudaError_t e = cudaMalloc(&p, count * sizeof(T));
+    cudaError_t e = fail_this_allocation() ? cudaErrorMemoryAllocation : cudaMalloc(&p, count * sizeof(T));
     if (e != cudaSuccess) {
       *rc = cuda_fail(e, "cudaMalloc");
       return nullptr;
@@ -1306,6 +1319,21 @@ int create_impl(const gpt_config_t* cfg, const gpt_weights_t* w, void* stream, g
 // ====================================================================== C ABI
 
 namespace {
+// One CTA waits on an mbarrier, with the bounded wait every pipeline in the library uses, for
+// at most limit_ns; arrive = 0 leaves the barrier without an arrival, so the wait runs out.
+__global__ void wait_probe_kernel(unsigned long long limit_ns, int arrive, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (arrive) mbar_arrive(&bar);
+    mbar_wait_limit(&bar, 0, err, limit_ns);
+  }
+}
+
 // Pointer alignment the stand-alone entry points check before any launch (their kernels use
 // vector loads and stores of that width).
 bool aligned(const void* p, uintptr_t bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
@@ -1878,6 +1906,25 @@ int gpt_op_status(void) {
   return map_error_word(w);
 }
 
+// ------------------------------------------------------------------ failure-detection hooks
+
+int gpt_debug_bounded_wait(int32_t limit_us, int32_t arrive, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return GPT_EINVAL;
+  OpCtx* c = nullptr;
+  int rc = op_ctx(&c, 0, 0);
+  if (rc) return rc;
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<unsigned long long>(limit_us) * 1000ull, arrive ? 1 : 0, c->err);
+  CK(cudaGetLastError());
+  return GPT_OK;
+}
+
+int gpt_debug_fail_allocation(int32_t k) {
+  if (k < 0) return GPT_EINVAL;
+  g_fail_alloc_countdown.store(k);
+  return GPT_OK;
+}
+
 // ------------------------------------------------------------------ decode attention without allocation
 //
 // For callers that must not allocate device memory: a host process whose allocator owns
@@ -1903,12 +1950,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 unsigned char* g_noalloc_addr[64] = {};
 std::mutex g_noalloc_mu;
 
-int noalloc_scratch(unsigned char** out) {
+// The cached address is that of the device's primary context when it was looked up: a
+// cudaDeviceReset (or any reset of the primary context) leaves it stale.
+int noalloc_scratch(unsigned char** out, cudaStream_t st) {
   int dev = 0;
   CK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return GPT_EUNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (!g_noalloc_addr[dev]) {
+    // The look-up is not a stream operation; inside a stream capture it could invalidate the
+    // capture, so a first call on a device while `st` is capturing is refused.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CK(cudaStreamIsCapturing(st, &cs));
+    if (cs != cudaStreamCaptureStatusNone) {
+      g_detail = "gpt_attention_decode_noalloc: the first call on a device must come before any stream capture";
+      return GPT_EUNSUPPORTED;
+    }
     void* p = nullptr;
     CK(cudaGetSymbolAddress(&p, g_noalloc_scratch));
     g_noalloc_addr[dev] = static_cast<unsigned char*>(p);
@@ -1939,10 +1996,10 @@ int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void*
                " bytes (max " + std::to_string(NOALLOC_PARTIAL_BYTES) + ")";
     return GPT_ETOOBIG;
   }
-  unsigned char* base = nullptr;
-  int rc = noalloc_scratch(&base);
-  if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char* base = nullptr;
+  int rc = noalloc_scratch(&base, st);
+  if (rc) return rc;
   unsigned int* tickets = reinterpret_cast<unsigned int*>(base + NOALLOC_TICKET_OFFSET);
   float* ws = reinterpret_cast<float*>(base + NOALLOC_PARTIAL_OFFSET);
   int* err = err_dev ? err_dev : reinterpret_cast<int*>(base);

@@ -34,6 +34,7 @@ EXPORTED = (
     "gpt_cache_length", "gpt_kernel_launches", "gpt_sync_status", "gpt_strerror", "gpt_last_error_detail", "gpt_linear_bf16",
     "gpt_layernorm", "gpt_attention_prefill", "gpt_attention_decode", "gpt_sample", "gpt_op_status",
     "gpt_attention_decode_noalloc", "gpt_linear_decode_bf16", "gpt_layernorm_linear_decode_bf16", "gpt_profile_gemms", "gpt_gemm_timing",
+    "gpt_debug_bounded_wait", "gpt_debug_fail_allocation",
 )
 
 c_int32, c_void_p, c_float, c_uint64, c_int64 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float, ctypes.c_uint64, ctypes.c_int64
@@ -115,6 +116,8 @@ def lib() -> ctypes.CDLL:
             "gpt_sample": (ctypes.c_int, [c_void_p, c_int32, c_int32, c_float, c_int32, c_uint64, c_int32, c_void_p,
                                           c_void_p, c_void_p, c_void_p]),
             "gpt_op_status": (ctypes.c_int, []),
+            "gpt_debug_bounded_wait": (ctypes.c_int, [c_int32, c_int32, c_void_p]),
+            "gpt_debug_fail_allocation": (ctypes.c_int, [c_int32]),
             "gpt_attention_decode_noalloc": (ctypes.c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                                             c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                                             c_void_p, c_void_p]),
@@ -301,6 +304,16 @@ def gpt_sample(logits: torch.Tensor, temperature: float, top_k: int | None, seed
 
 def gpt_op_status() -> int:
     return lib().gpt_op_status()
+
+
+def gpt_debug_bounded_wait(limit_us: int, arrive: bool) -> None:
+    """Launch the bounded-wait probe (arrive=False lets the wait run out: GPT_ETIMEOUT)."""
+    _check(lib().gpt_debug_bounded_wait(limit_us, 1 if arrive else 0, _stream()), "gpt_debug_bounded_wait")
+
+
+def gpt_debug_fail_allocation(k: int) -> None:
+    """Fail the k-th next model allocation (0: off)."""
+    _check(lib().gpt_debug_fail_allocation(k), "gpt_debug_fail_allocation")
 
 
 def gpt_attention_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pos0: torch.Tensor,

@@ -85,19 +85,27 @@ def test_gpt2_124m_b1_greedy_teacher_forced():
     assert agree >= 0.99
 
 
-@pytest.mark.parametrize("name,rows", [("gpt2_124m_b64_p512_d512", [0, 21, 63]), ("gpt2_350m_b8_p768_d256", [0, 7])])
+@pytest.mark.parametrize("name,rows", [("gpt2_124m_b64_p512_d512", [0, 21, 42, 63]),
+                                       ("gpt2_350m_b8_p768_d256", [0, 7])])
 def test_full_size_sampled_rows(name, rows):
-    """Full batch and cache at the benchmark's sizes; sampled rows are checked at every
-    position against the oracle's no-cache forward over the whole fed sequence."""
+    """Full batch and cache at the benchmark's sizes.  The prefill's logits are checked for
+    every row of the batch; sampled rows are then checked at every decode position against
+    the oracle's no-cache forward over the whole fed sequence."""
     wl = syn.WORKLOADS[name]
     sd = _weights(wl)
     prompt = syn.make_tokens(wl.batch, wl.prompt, wl.token_hi)
     forced = syn.make_tokens(wl.batch, wl.decode_steps, wl.token_hi, seed=77)
     model = make_gpu_model(wl.model, sd, wl.batch)
+    pre_all = model.prefill(torch.from_numpy(prompt).cuda()).cpu().numpy()  # (B, V), every row
     got = gpu_teacher_forced(model, prompt, forced, rows=rows)  # (N+1, rows, V)
     assert model.cache_length == wl.prompt + wl.decode_steps == wl.model.block_size
     del model
     cfg, w = oracle_model(wl.model, sd)
+    pre_ref = np.concatenate([og.prefill(cfg, w, prompt[b:b + 8])[0] for b in range(0, wl.batch, 8)])
+    pre_err = np.max(np.abs(pre_all - pre_ref))
+    print(f"{name}: prefill of all {wl.batch} rows: max|err| {pre_err:.3e}")
+    assert pre_err < BF16_TOL
+    assert argmax_agreement(pre_all, pre_ref) >= 0.99
     errs, agree = [], []
     for i, r in enumerate(rows):
         seq = np.concatenate([prompt[r:r + 1], forced[r:r + 1]], axis=1)
@@ -139,6 +147,57 @@ def test_generate_matches_step_by_step_and_oracle_sampler():
     # a second generate reuses the captured graph and gives the same tokens
     out2 = model.generate(prompt, N, temperature=temp, top_k=k, seed=seed)
     assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("B", [64, 33])  # 33: chains of 16 and 17 sequences
+def test_generate_at_the_benchmark_configuration(B):
+    """The path the benchmark times: GPT-2 124M, prompt 512, temperature 1.0, top_k 50, per-row
+    Philox streams, with 40 draws.  (a) gpt_generate's tokens equal the step-by-step chain
+    gpt_prefill -> [gpt_sample -> gpt_decode_step] with the same seed and draw indices; (b) each
+    draw of the first and last row of both decode chains equals the oracle's sampler applied to
+    the GPU logits of that step; (c) those logits match the oracle's no-cache forward over the
+    generated sequence (teacher-forced), within the bf16 tolerance and >= 99% argmax agreement.
+    ("原生 nanoGPT 模型服务首选", §2 generate(); "极速上手nanoGPT", §关键参数: temperature, top_k.)"""
+    wl = syn.WORKLOADS["gpt2_124m_b64_p512_d512"]
+    sd = _weights(wl)
+    N, seed = 40, 20240
+    P, temp, k = wl.prompt, wl.temperature, wl.top_k
+    prompt = syn.make_tokens(wl.batch, P, wl.token_hi)[:B].copy()
+    pd = torch.from_numpy(prompt).cuda()
+    model = make_gpu_model(wl.model, sd, wl.batch)
+    out = model.generate(pd, N, temperature=temp, top_k=k, seed=seed)
+    assert model.sync_status() == G.GPT_OK
+    assert torch.equal(out[:, :P], pd)
+    B0 = B // 2
+    rows = [0, B0 - 1, B0, B - 1]  # first and last rows of both chains
+    logits = model.prefill(pd)
+    toks, kept = [], []
+    for j in range(N):
+        tok = torch.empty(B, dtype=torch.int32, device="cuda")
+        G.gpt_sample(logits, temp, k, seed, j, tok)
+        toks.append(tok)
+        lg = logits[rows].cpu().numpy()
+        kept.append(lg)
+        t_host = tok.cpu().numpy()
+        for i, r in enumerate(rows):
+            assert t_host[r] == osm.sample_row(lg[i], temp, k, seed, r, j), (r, j)
+        if j + 1 < N:
+            logits = model.decode_step(tok)
+    assert model.sync_status() == G.GPT_OK
+    assert torch.equal(out[:, P:], torch.stack(toks, dim=1))
+    gen = out.cpu().numpy()
+    del model
+    cfg, w = oracle_model(wl.model, sd)
+    got = np.stack(kept)  # (N, rows, V): logits before draw j
+    errs, agree = [], []
+    for i, r in enumerate(rows):
+        full = og.forward_full(cfg, w, gen[r:r + 1, :P + N - 1])[0, P - 1:]  # positions P-1 .. P+N-2
+        errs.append(np.max(np.abs(got[:, i] - full)))
+        agree.append(np.argmax(got[:, i], axis=-1) == np.argmax(full, axis=-1))
+    agree = float(np.mean(np.concatenate(agree)))
+    print(f"generate B={B}: max|err| {max(errs):.3e}, argmax agreement {agree:.4f}")
+    assert max(errs) < BF16_TOL
+    assert agree >= 0.99
 
 
 def test_generate_greedy_equals_oracle_greedy_on_fp32_model():
@@ -408,3 +467,23 @@ def test_paged_cache_reports_an_exhausted_pool():
         model.extend(torch.zeros(1, 64, dtype=torch.int32, device="cuda"))  # a fourth page
     assert ex.value.code == G.GPT_ENOMEM
     assert model.sync_status() == G.GPT_OK
+
+
+def test_model_from_an_hf_layout_checkpoint():
+    """A checkpoint in the HF GPT-2 layout (Conv1D weights, mask buffers, tied lm_head, zero
+    biases of a bias=False model), converted on the host, gives bit-identical logits to the
+    model built from the nanoGPT-named weights."""
+    from kv_cached_generation_gpt_b300 import checkpoint as ck
+
+    shape = syn.ModelShape(2, 2, 128, 64, 300, False, "bf16")
+    sd = syn.make_weights(shape, seed=51, random_gamma=True)
+    config, conv = ck.from_hf_state_dict(ck.to_hf_state_dict(sd, shape.n_layer), n_head=shape.n_head,
+                                         drop_zero_bias=True)
+    assert config["bias"] is False and config["vocab_size"] == 300
+    prompt = torch.from_numpy(syn.make_tokens(2, 20, 300, seed=52)).cuda()
+    a = make_gpu_model(shape, sd, 2)
+    b = make_gpu_model(shape, conv, 2)
+    assert torch.equal(a.prefill(prompt), b.prefill(prompt))
+    tok = prompt[:, 0].contiguous()
+    assert torch.equal(a.decode_step(tok), b.decode_step(tok))
+    assert a.sync_status() == G.GPT_OK and b.sync_status() == G.GPT_OK
