@@ -270,7 +270,8 @@ int gpt_layernorm(const float* x, int64_t x_stride, const float* gamma, const fl
  * q (dev, dtype): B x n_head x T x hs.  k_cache, v_cache (dev, dtype): B x n_head x block x
  * hs, holding keys for positions 0 .. pos0+T-1.  Query t sits at position pos0 + t and sees
  * keys 0 .. pos0+t.  y (dev, dtype): (B*T) x (hs*n_head), row b*T + t, column h*hs + d.
- * bf16 runs on tensor cores (mma.sync), fp32 exactly in fp32 (pos0 + T <= 12288).
+ * bf16 runs on the tcgen05 tensor cores (S and O in TMEM, Q/K/V tiles by TMA), fp32 exactly
+ * in fp32 (pos0 + T <= 12288).
  * q, k_cache and v_cache 16-byte aligned. */
 int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
                           int32_t n_head, int32_t head_size, int32_t T, int32_t block, int32_t pos0, void* y,

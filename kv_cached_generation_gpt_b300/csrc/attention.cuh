@@ -12,8 +12,8 @@
 //   attn_decode_kernel  -- one new query per (b, h); split-KV over the keys, 8 lanes per key
 //                          with 128-bit loads, warp-shuffle reductions, online softmax in
 //                          fp32, splits merged by log-sum-exp in a fixed order.
-//   attn_prefill_bf16   -- FlashAttention-style tiles: 64 queries x 64 keys per step on
-//                          mma.sync m16n8k16 (bf16 in, fp32 accumulate), online softmax.
+//   attn_prefill_tc     -- FlashAttention-style tiles on tcgen05: 128 queries x 64 keys per
+//                          step, S and O accumulated in TMEM, online softmax in fp32.
 //   attn_prefill_f32    -- exact fp32 path for fp32 models (warp per query).
 #pragma once
 
@@ -26,8 +26,15 @@ constexpr float LOG2E_F = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ decode
 
-constexpr int DEC_THREADS = 128;  // 4 warps
-constexpr int DEC_UNROLL = 4;     // keys per lane group per iteration
+#ifndef KVGPT_DEC_WARPS
+#define KVGPT_DEC_WARPS 4
+#endif
+constexpr int DEC_WARPS = KVGPT_DEC_WARPS;
+constexpr int DEC_THREADS = 32 * DEC_WARPS;
+#ifndef KVGPT_DEC_UNROLL
+#define KVGPT_DEC_UNROLL 4
+#endif
+constexpr int DEC_UNROLL = KVGPT_DEC_UNROLL;  // keys per lane group per iteration
 
 template <typename T>
 struct Vec8;  // 8 consecutive head dims of one row
@@ -83,9 +90,9 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
   static_assert(HSZ == 32 || HSZ == 64, "head size 32 or 64");
   constexpr int LPK = HSZ / 8;        // lanes per key
   constexpr int KPW = 32 / LPK;       // keys per warp per load
-  constexpr int KPI = 4 * KPW;        // keys per CTA per unrolled slot
-  __shared__ float s_m[4], s_l[4];
-  __shared__ float s_acc[4][HSZ];
+  constexpr int KPI = DEC_WARPS * KPW;  // keys per CTA per unrolled slot
+  __shared__ float s_m[DEC_WARPS], s_l[DEC_WARPS];
+  __shared__ float s_acc[DEC_WARPS][HSZ];
   __shared__ int s_last;
   const int bh = blockIdx.x, split = blockIdx.y, splits = gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,8 +197,8 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
   float M = -INFINITY, L = 0.0f, A = 0.0f;
   const int d = threadIdx.x;
   if (d < HSZ) {
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, s_m[w]);
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, s_m[w]);
+    for (int w = 0; w < DEC_WARPS; ++w) {
       const float c = (s_m[w] == -INFINITY) ? 0.0f : exp2f(s_m[w] - M);
       L += s_l[w] * c;
       A += s_acc[w][d] * c;
@@ -239,213 +246,287 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(const T* __res
   if (threadIdx.x == 0) tickets[bh] = 0u;
 }
 
-// ------------------------------------------------------------------ prefill, bf16 tensor cores
+// ------------------------------------------------------------------ prefill, tcgen05
 
-constexpr int PF_BQ = 64, PF_BKEY = 64, PF_THREADS = 128;  // 4 warps x 16 query rows
+// FlashAttention-style causal prefill on the Blackwell tensor core.  One CTA takes 128 query rows
+// of one (b, h) and walks key tiles of 64:
+//   S = Q K^T          tcgen05.mma M=128 N=64 K=64, fp32 in TMEM columns [0, 64)
+//   softmax            warps 0-3, thread = query row = TMEM lane: scale, causal mask, running
+//                      max and sum (fp32); P = exp2(s - m) as bf16 into shared memory
+//   O += P V           tcgen05.mma M=128 N=64 K=64 keys, V read as an MN-major operand (the
+//                      cache rows are [key][dim]), fp32 in TMEM columns [64, 128)
+// Q, K and V tiles arrive by TMA (128-byte swizzle) from the q buffer and the cache rows of the
+// (b, h), found through KvLayout (a 64-key tile never straddles a page).  The MMA warp issues
+// S for tile j+1 as soon as the softmax warps have read S for tile j, so the softmax of tile j
+// overlaps the MMAs of tiles j-1 and j+1; K/V run four tiles ahead; two CTAs per SM overlap
+// further.  The running max is raised lazily: O (in TMEM) and the sum are
+// rescaled only when a row's max grows by more than 2^8, so p = exp2(s - m) stays <= 256 and
+// most tiles skip the TMEM round trip (y = O / l is exact for any m used consistently).
+// Keys at or past pos0 + T in the last tile are zeroed in V before P V (the cache may hold
+// anything there) and masked in S.
+constexpr int PT_BQ = 128;       // query rows per CTA (MMA M)
+constexpr int PT_BK = 64;        // keys per tile
+constexpr int PT_THREADS = 192;  // warps 0-3 softmax + output, warp 4 TMA, warp 5 MMA
+constexpr uint32_t PT_Q_BYTES = PT_BQ * HS * 2;
+constexpr uint32_t PT_KV_BYTES = PT_BK * HS * 2;
+constexpr uint32_t PT_P_BYTES = PT_BQ * PT_BK * 2;
+constexpr int PT_STAGES = 4;     // K/V ring
+constexpr uint32_t PT_SMEM = 1024 + PT_Q_BYTES + 2 * PT_STAGES * PT_KV_BYTES + PT_P_BYTES + 256;
+constexpr float PT_RESCALE_LOG2 = 8.0f;
 
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Byte offset of 16-byte chunk c of row r in a 64 x 64 bf16 tile with XOR swizzle.
-__device__ __forceinline__ uint32_t swz(int r, int c) { return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4)); }
-
-// Copy ROWS consecutive rows of 64 bf16 starting at src into a swizzled tile; rows >= nvalid are zeros.
-template <int ROWS>
-__device__ __forceinline__ void load_tile64(uint32_t tile, const __nv_bfloat16* src, int nvalid) {
-#pragma unroll
-  for (int i = 0; i < ROWS * 8 / PF_THREADS; ++i) {
-    const int idx = threadIdx.x + i * PF_THREADS;  // ROWS x 8 chunks of 16 B
-    const int r = idx >> 3, c = idx & 7;
-    const bool ok = r < nvalid;
-    const __nv_bfloat16* p = src + static_cast<size_t>(ok ? r : 0) * HS + c * 8;
-    cp_async16(tile + swz(r, c), p, ok);
-  }
+// 2^x by the SFU's approximate instruction (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-// grid (ceil(T/64), B*nh).  Queries t in [0, T) sit at positions pos0 + t; keys 0..pos0+T-1.
-// Query blocks run heaviest (most keys) first: block qb = gridDim.x - 1 - blockIdx.x.
-__global__ void __launch_bounds__(PF_THREADS) attn_prefill_bf16(const __nv_bfloat16* __restrict__ q,
-                                                                const __nv_bfloat16* __restrict__ kc,
-                                                                const __nv_bfloat16* __restrict__ vc, KvLayout kv,
-                                                                int nh, int T,
-                                                                int block, int pos0, __nv_bfloat16* __restrict__ y,
-                                                                int C) {
-  __shared__ __align__(128) __nv_bfloat16 sQ[PF_BQ * HS];
-  __shared__ __align__(128) __nv_bfloat16 sK[2][PF_BKEY * HS];
-  __shared__ __align__(128) __nv_bfloat16 sV[2][PF_BKEY * HS];
-  const int qb = gridDim.x - 1 - blockIdx.x, bh = blockIdx.y;
+// grid (ceil(T/128), B*nh), PT_THREADS threads, PT_SMEM dynamic shared memory.  tmQ: q as
+// [B*nh*T][64] rows; tmK / tmV: one layer's cache as [rows][64] (KvLayout::row numbering);
+// 128-row (q) and 64-row (cache) boxes of 64 columns with 128-byte swizzle.  Queries t in [0, T)
+// sit at positions pos0 + t and see keys 0 .. pos0 + t.
+__global__ void __launch_bounds__(PT_THREADS, 2) attn_prefill_tc(const __grid_constant__ CUtensorMap tmQ,
+                                                               const __grid_constant__ CUtensorMap tmK,
+                                                               const __grid_constant__ CUtensorMap tmV, KvLayout kv,
+                                                               int nh, int T, int pos0, __nv_bfloat16* __restrict__ y,
+                                                               int C, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + PT_Q_BYTES;                // PT_STAGES stages
+  uint8_t* sV = sK + PT_STAGES * PT_KV_BYTES;   // PT_STAGES stages
+  uint8_t* sP = sV + PT_STAGES * PT_KV_BYTES;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + PT_P_BYTES);
+  uint64_t* q_full = bar;
+  uint64_t* k_full = bar + 1;                  // [PT_STAGES]
+  uint64_t* v_full = k_full + PT_STAGES;       // [PT_STAGES]
+  uint64_t* kv_empty = v_full + PT_STAGES;     // [PT_STAGES]
+  uint64_t* s_full = kv_empty + PT_STAGES;
+  uint64_t* s_empty = s_full + 1;
+  uint64_t* p_full = s_empty + 1;
+  uint64_t* p_empty = p_full + 1;              // P V of the last tile is done (P and O are free)
+  uint64_t* drain = p_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int q0 = qb * PF_BQ;
-  const int n_keys = pos0 + T;
-  const int last_key = min(pos0 + q0 + PF_BQ - 1, n_keys - 1);
-  const int n_kb = last_key / PF_BKEY + 1;
-  const __nv_bfloat16* qg = q + static_cast<size_t>(bh) * T * HS;
-  const int bq = bh / nh, hq = bh - bq * nh;
-  // keys r .. r+63 of this (b, h), r a multiple of 64: consecutive rows (pages hold >= 64)
-  auto krows = [&](int r) { return kc + kv.row(bq, hq, r) * HS; };
-  auto vrows = [&](int r) { return vc + kv.row(bq, hq, r) * HS; };
-  constexpr uint32_t TILE_BYTES = PF_BKEY * HS * 2;
-  const uint32_t sq = smem_u32(sQ), sk0 = smem_u32(sK[0]), sv0 = smem_u32(sV[0]);
+  const int qt = gridDim.x - 1 - blockIdx.x, bh = blockIdx.y;  // heaviest query tiles first
+  const int q0 = qt * PT_BQ;
+  const int b = bh / nh, h = bh - b * nh;
+  const int kv_len = pos0 + T;
+  const int last_q = min(q0 + PT_BQ, T) - 1;
+  const int nk = (pos0 + last_q) / PT_BK + 1;
 
-  load_tile64<PF_BQ>(sq, qg + static_cast<size_t>(q0) * HS, T - q0);
-  load_tile64<PF_BKEY>(sk0, krows(0), n_keys);
-  load_tile64<PF_BKEY>(sv0, vrows(0), n_keys);
-  cp_async_commit();
-
-  uint32_t qa[4][4];  // A fragments of this warp's 16 query rows, 4 k-steps of 16 dims
-  float o[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[i][j] = 0.0f;
-  float row_m[2] = {-INFINITY, -INFINITY}, row_l[2] = {0.0f, 0.0f};
-  const float sc = 0.125f * LOG2E_F;
-  const int qpos0 = pos0 + q0 + warp * 16 + gq;  // absolute position of row gq (row gq+8 is +8)
-
-  for (int kb = 0; kb < n_kb; ++kb) {
-    const int buf = kb & 1;
-    const uint32_t skb = sk0 + buf * TILE_BYTES, svb = sv0 + buf * TILE_BYTES;
-    if (kb + 1 < n_kb) {
-      load_tile64<PF_BKEY>(sk0 + (buf ^ 1) * TILE_BYTES, krows((kb + 1) * PF_BKEY), n_keys - (kb + 1) * PF_BKEY);
-      load_tile64<PF_BKEY>(sv0 + (buf ^ 1) * TILE_BYTES, vrows((kb + 1) * PF_BKEY), n_keys - (kb + 1) * PF_BKEY);
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < PT_STAGES; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
     }
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (kb == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        // matrices: rows 0-7 / 8-15 of the warp's 16 rows x dims [16ks, 16ks+8) / [16ks+8, 16ks+16)
-        const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = ks * 2 + (lane >> 4);
-        ldmatrix_x4(qa[ks], sq + swz(r, c));
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 128);
+    mbar_init(p_full, 128);
+    mbar_init(p_empty, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 64;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, PT_Q_BYTES);
+      tma_load_2d(&tmQ, q_full, sQ, 0, bh * T + q0);
+      int issued = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int st = j % PT_STAGES;
+        if (j >= PT_STAGES && !mbar_wait(&kv_empty[st], ((j / PT_STAGES) & 1) ^ 1, err)) break;
+        const int row = static_cast<int>(kv.row(b, h, j * PT_BK));
+        mbar_arrive_expect_tx(&k_full[st], PT_KV_BYTES);
+        tma_load_2d(&tmK, &k_full[st], sK + st * PT_KV_BYTES, 0, row);
+        mbar_arrive_expect_tx(&v_full[st], PT_KV_BYTES);
+        tma_load_2d(&tmV, &v_full[st], sV + st * PT_KV_BYTES, 0, row);
+        issued = j + 1;
+      }
+      // every load has landed before the CTA may exit
+      mbar_wait(q_full, 0, err);
+      for (int j = max(0, issued - PT_STAGES); j < issued; ++j) {
+        mbar_wait(&k_full[j % PT_STAGES], (j / PT_STAGES) & 1, err);
+        mbar_wait(&v_full[j % PT_STAGES], (j / PT_STAGES) & 1, err);
       }
     }
-    // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
-    float s[8][4];
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(PT_BQ, PT_BK);
+      const uint32_t id_pv = idesc_bf16_f32(PT_BQ, HS) | (1u << 16);  // B (V) is MN-major
+      const uint32_t aq = smem_u32(sQ), ap = smem_u32(sP);
+      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(&k_full[0], 0, err);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s[nt][j] = 0.0f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t kf[4];
-        const int r = nt * 8 + (lane & 7);
-        const int c = half * 4 + (lane >> 3);
-        ldmatrix_x4(kf, skb + swz(r, c));
-        mma_bf16_16816(s[nt], qa[half * 2], kf[0], kf[1]);
-        mma_bf16_16816(s[nt], qa[half * 2 + 1], kf[2], kf[3]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tS, sdesc_sw128(aq + 32 * ks), sdesc_sw128(smem_u32(sK) + 32 * ks), id_s, ks != 0);
+        umma_commit(s_full);
       }
-    }
-    // scale, causal mask, online softmax (rows gq and gq+8 of the warp's 16)
-    const int kbase = kb * PF_BKEY;
-    const bool need_mask = kbase + PF_BKEY - 1 > pos0 + q0 + warp * 16;
-    float mx[2] = {row_m[0], row_m[1]};
+      for (int j = 0; j < nk && ok; ++j) {
+        const int st = j % PT_STAGES;
+        if (j + 1 < nk) {
+          const int s1 = (j + 1) % PT_STAGES;
+          if (!(ok = mbar_wait(s_empty, j & 1, err) && mbar_wait(&k_full[s1], ((j + 1) / PT_STAGES) & 1, err))) break;
+          tc_fence_after();
+          const uint32_t bk = smem_u32(sK + s1 * PT_KV_BYTES);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float v = s[nt][j] * sc;
-        if (need_mask) {
-          const int key = kbase + nt * 8 + tq * 2 + (j & 1);
-          const int qp = qpos0 + (j >> 1) * 8;
-          if (key > qp) v = -INFINITY;
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tS, sdesc_sw128(aq + 32 * ks), sdesc_sw128(bk + 32 * ks), id_s, ks != 0);
+          umma_commit(s_full);
         }
-        s[nt][j] = v;
-        mx[j >> 1] = fmaxf(mx[j >> 1], v);
+        if (!(ok = mbar_wait(p_full, j & 1, err) && mbar_wait(&v_full[st], (j / PT_STAGES) & 1, err))) break;
+        tc_fence_after();
+        const uint32_t bv = smem_u32(sV + st * PT_KV_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // 16 keys per step: 2 swizzle atoms of 8 key rows
+          umma_bf16(tO, sdesc_sw128(ap + 32 * ks), sdesc_sw128(bv + 2048 * ks), id_pv, (j | ks) != 0);
+        umma_commit(p_empty);
+        umma_commit(&kv_empty[st]);
+      }
+      umma_commit(drain);  // no MMA of this CTA is in flight once it completes
+      mbar_wait(drain, 0, err);
+    }
+  } else {
+    // softmax warps: thread = query row r of the tile
+    const int r = warp * 32 + lane;
+    const int qi = q0 + r;
+    const bool valid = qi < T;
+    const int qpos = pos0 + qi;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sc = 0.125f * LOG2E_F;
+    float m_used = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!(ok = mbar_wait(s_full, j & 1, err))) break;
+      tc_fence_after();
+      float s[PT_BK];
+      {
+        // the four 16-column loads in flight together, one wait
+        uint32_t r0[16], r1[16], r2[16], r3[16];
+        tmem_ld16_raw(tS + lane_base, r0);
+        tmem_ld16_raw(tS + lane_base + 16, r1);
+        tmem_ld16_raw(tS + lane_base + 32, r2);
+        tmem_ld16_raw(tS + lane_base + 48, r3);
+        tmem_wait_ld16(r0, r1);
+        tmem_wait_ld16(r2, r3);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[16 + i] = __uint_as_float(r1[i]);
+          s[32 + i] = __uint_as_float(r2[i]);
+          s[48 + i] = __uint_as_float(r3[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_empty);
+      const int kbase = j * PT_BK;
+      // causal mask (and rows past T): only tiles reaching past the warp's first query position
+      if (__any_sync(0xffffffffu, !valid || kbase + PT_BK - 1 > qpos)) {
+#pragma unroll
+        for (int c = 0; c < PT_BK; ++c)
+          if (!valid || kbase + c > qpos) s[c] = -INFINITY;
+      }
+      // row max of the raw scores in 8 independent chains, then scaled (sc > 0)
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < PT_BK; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mx = mraw * sc;
+      const bool need = mx > m_used + PT_RESCALE_LOG2 || (m_used == -INFINITY && mx > -INFINITY);
+      // P and O are free once P V of tile j-1 is done (every phase is waited, in order)
+      if (j >= 1 && !(ok = mbar_wait(p_empty, (j - 1) & 1, err))) break;
+      if (__any_sync(0xffffffffu, need && j > 0)) {
+        // O *= exp2(m_used - mx) on the rows whose max moved (warp-wide TMEM round trip)
+        const float corr = (need && j > 0) ? exp2f(m_used - mx) : 1.0f;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HS; c += 16) {
+          float t[16];
+          tmem_ld16(tO + lane_base + c, t);
+          uint32_t u[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(t[i] * corr);
+          tmem_st16(tO + lane_base + c, u);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      if (need) {
+        l = (m_used == -INFINITY) ? 0.0f : l * exp2f(m_used - mx);
+        m_used = mx;
+      }
+      // P = exp2(s * sc - m) (bf16) into row r of the 128 x 64 tile, 128-byte
+      // swizzle; the row sum in 8 independent chains.  A row without any visible key so far
+      // (only rows past T) gets P = 0.
+      const uint32_t prow = smem_u32(sP) + static_cast<uint32_t>(r * 128);
+      const bool live = m_used != -INFINITY;
+      const float neg_m = live ? -m_used : 0.0f;
+      float ps8[8];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = live ? ex2_approx(fmaf(s[ch * 8 + i], sc, neg_m)) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ps8[i] = ch == 0 ? p[i] : ps8[i] + p[i];
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + static_cast<uint32_t>((ch ^ (r & 7)) << 4)),
+                     "r"(pack_bf16x2(p[0], p[1])), "r"(pack_bf16x2(p[2], p[3])), "r"(pack_bf16x2(p[4], p[5])),
+                     "r"(pack_bf16x2(p[6], p[7]))
+                     : "memory");
+      }
+      l += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      if (j == nk - 1 && kbase + PT_BK > kv_len) {
+        // keys past the live cache: zero their V rows (0 * NaN would poison O)
+        const int st = j % PT_STAGES;
+        if (!(ok = mbar_wait(&v_full[st], (j / PT_STAGES) & 1, err))) break;
+        const uint32_t vb = smem_u32(sV + st * PT_KV_BYTES);
+        const int first = kv_len - kbase;
+        for (int i = r; i < (PT_BK - first) * 8; i += 128)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + static_cast<uint32_t>((first + i / 8) * 128 + (i % 8) * 16)),
+                       "r"(0u)
+                       : "memory");
+      }
+      fence_proxy_async_smem();  // the MMA reads P (and V) through the async proxy
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait(p_empty, (nk - 1) & 1, err)) {  // the last P V is done
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* dst = y + (static_cast<size_t>(b) * T + qi) * C + h * HS;
+#pragma unroll
+      for (int c = 0; c < HS; c += 16) {
+        float t[16];
+        tmem_ld16(tO + lane_base + c, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[i] *= inv;
+        if (valid) store16(dst + c, t);
       }
     }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-    }
-    float corr[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      corr[h] = (mx[h] == -INFINITY) ? 1.0f : exp2f(row_m[h] - mx[h]);
-      row_m[h] = mx[h];
-      row_l[h] *= corr[h];
-    }
-#pragma unroll
-    for (int dn = 0; dn < 8; ++dn) {
-      o[dn][0] *= corr[0];
-      o[dn][1] *= corr[0];
-      o[dn][2] *= corr[1];
-      o[dn][3] *= corr[1];
-    }
-    uint32_t pa[4][4];  // P as A fragments, 4 k-steps of 16 keys
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      float p[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float mm = row_m[j >> 1];
-        p[j] = (mm == -INFINITY) ? 0.0f : exp2f(s[nt][j] - mm);
-        row_l[j >> 1] += p[j];
-      }
-      const int ks = nt >> 1, hi = nt & 1;
-      pa[ks][hi * 2 + 0] = pack_bf16x2(p[0], p[1]);
-      pa[ks][hi * 2 + 1] = pack_bf16x2(p[2], p[3]);
-    }
-    // O += P V: 8 n-tiles of 8 dims, 4 k-steps of 16 keys
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-      for (int dp = 0; dp < 4; ++dp) {  // pairs of dim n-tiles
-        uint32_t vf[4];
-        const int r = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = dp * 2 + (lane >> 4);
-        ldmatrix_x4_trans(vf, svb + swz(r, c));
-        mma_bf16_16816(o[dp * 2], pa[ks], vf[0], vf[1]);
-        mma_bf16_16816(o[dp * 2 + 1], pa[ks], vf[2], vf[3]);
-      }
-    }
-    __syncthreads();
   }
-  cp_async_wait<0>();
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    row_l[h] += __shfl_xor_sync(0xffffffffu, row_l[h], 1);
-    row_l[h] += __shfl_xor_sync(0xffffffffu, row_l[h], 2);
-  }
-  const int b = bh / nh, hh = bh - b * nh;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = q0 + warp * 16 + gq + h * 8;
-    if (t < T) {
-      const float inv = 1.0f / row_l[h];
-      __nv_bfloat16* yr = y + (static_cast<size_t>(b) * T + t) * C + hh * HS;
-#pragma unroll
-      for (int dn = 0; dn < 8; ++dn) {
-        *reinterpret_cast<uint32_t*>(yr + dn * 8 + tq * 2) = pack_bf16x2(o[dn][h * 2] * inv, o[dn][h * 2 + 1] * inv);
-      }
-    }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
   }
 }
 

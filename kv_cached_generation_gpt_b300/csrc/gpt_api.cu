@@ -235,6 +235,22 @@ cudaError_t init_persist_attrs_once() {
   return cudaSuccess;
 }
 
+// The tcgen05 prefill attention's shared-memory limit, once per device (for the stand-alone
+// operation; gpt_create sets it with the other kernels').
+cudaError_t init_attn_tc_once() {
+  static unsigned long long mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t r = cudaGetDevice(&dev);
+  if (r != cudaSuccess) return r;
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 64 && (mask & (1ull << dev))) return cudaSuccess;
+  r = cudaFuncSetAttribute(attn_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PT_SMEM));
+  if (r != cudaSuccess) return r;
+  if (dev < 64) mask |= 1ull << dev;
+  return cudaSuccess;
+}
+
 template <int BN, int EPI>
 cudaError_t launch_persist_epi(const CUtensorMap& ta, const CUtensorMap& tb, int K, int grid, const Epi<bf16>& e,
                                cudaStream_t st) {
@@ -435,6 +451,8 @@ cudaError_t init_kernel_attrs(int dev) {
         if (r != cudaSuccess) return r;
       }
   cudaError_t r = init_persist_attrs();
+  if (r != cudaSuccess) return r;
+  r = cudaFuncSetAttribute(attn_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PT_SMEM));
   if (r != cudaSuccess) return r;
   return init_dl_attrs(dev);
 }
@@ -998,8 +1016,15 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
                     static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
                     static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
     } else if constexpr (kBf16) {
-      attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * nh), PF_THREADS, 0, st>>>(q, kc, vc, kvl, nh, T, m->block,
-                                                                             off, y, C);
+      // q [B][nh][T][64] and this layer's cache rows as 2-D tensors for TMA
+      const long long cache_rows = static_cast<long long>(m->cache_layer_bytes() / (m->hs * m->esz));
+      CUtensorMap tq, tk, tv;
+      int rc = m->weight_map(q, static_cast<long long>(B) * nh * T, m->hs, PT_BQ, &tq);
+      if (!rc) rc = m->weight_map(m->kcache(l), cache_rows, m->hs, PT_BK, &tk);
+      if (!rc) rc = m->weight_map(m->vcache(l), cache_rows, m->hs, PT_BK, &tv);
+      if (rc) return rc;
+      attn_prefill_tc<<<dim3(cdiv(T, PT_BQ), B * nh), PT_THREADS, PT_SMEM, st>>>(tq, tk, tv, kvl, nh, T, off, y, C,
+                                                                                m->d_err);
     } else {
       if (m->hs == 64)
         attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, kvl, nh, T,
@@ -1839,9 +1864,18 @@ int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cach
   kvl.nh = n_head;
   kvl.block = block;
   if (dtype == GPT_DTYPE_BF16) {
-    attn_prefill_bf16<<<dim3(cdiv(T, PF_BQ), B * n_head), PF_THREADS, 0, st>>>(
-        static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache), static_cast<const bf16*>(v_cache), kvl,
-        n_head, T, block, pos0, static_cast<bf16*>(y), C);
+    if (!load_encode()) return GPT_EUNSUPPORTED;
+    CK(init_attn_tc_once());
+    OpCtx* ctx = nullptr;
+    int rc = op_ctx(&ctx, 0, 0);
+    if (rc) return rc;
+    CUtensorMap tq, tk, tv;
+    const long long rows = static_cast<long long>(B) * n_head * block;
+    if ((rc = make_tmap(&tq, q, static_cast<long long>(B) * n_head * T, head_size, PT_BQ))) return rc;
+    if ((rc = make_tmap(&tk, k_cache, rows, head_size, PT_BK))) return rc;
+    if ((rc = make_tmap(&tv, v_cache, rows, head_size, PT_BK))) return rc;
+    attn_prefill_tc<<<dim3(cdiv(T, PT_BQ), B * n_head), PT_THREADS, PT_SMEM, st>>>(tq, tk, tv, kvl, n_head, T, pos0,
+                                                                                   static_cast<bf16*>(y), C, ctx->err);
   } else if (dtype == GPT_DTYPE_F32) {
     if ((pos0 + T) * sizeof(float) > 48 * 1024) return GPT_EINVAL;
     auto kern = head_size == 64 ? attn_prefill_f32<64> : attn_prefill_f32<32>;

@@ -280,7 +280,9 @@ def _cache(r, B, nh, block, n, dt, hs=64):
 
 @pytest.mark.parametrize("dt,hs", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float32, 32)])
 @pytest.mark.parametrize("B,nh,T,pos0,block", [(1, 1, 1, 0, 8), (2, 3, 17, 0, 32), (1, 2, 64, 0, 64),
-                                               (2, 2, 100, 0, 128), (1, 12, 129, 0, 256), (2, 2, 37, 50, 128)])
+                                               (2, 2, 100, 0, 128), (1, 12, 129, 0, 256), (2, 2, 37, 50, 128),
+                                               (2, 2, 300, 0, 512), (1, 3, 200, 250, 512), (2, 12, 512, 0, 1024),
+                                               (1, 2, 129, 63, 200)])
 def test_attention_prefill_matches_oracle(dt, hs, B, nh, T, pos0, block):
     r = _rng(B * 100 + T + pos0)
     q = torch.from_numpy(r.standard_normal((B, nh, T, hs)).astype(np.float32)).to(dt).cuda()
