@@ -405,6 +405,20 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Decode attention over a grid of (rows x splits) CTAs: the 8-warp form for small grids, the
+// 4-warp form otherwise (DEC_WIDE_MAX_CTAS).  The choice depends on the shapes only, so every
+// entry point gives the same results for the same inputs.
+template <typename T, int HSZ, bool PAGED>
+cudaError_t launch_dec_attn(int rows, int splits, cudaStream_t st, const T* q, const T* kc, const T* vc,
+                            const KvLayout& kv, int nh, int block, const int* pos0, const int* pos_rows, float* ws,
+                            unsigned int* tickets, T* y, T* y_lo, int C, int* err) {
+  if (static_cast<long long>(rows) * splits <= DEC_WIDE_MAX_CTAS)
+    return launch_k(attn_decode_kernel<T, HSZ, PAGED, 8>, dim3(rows, splits), dim3(256), 0, st, false, q, kc, vc, kv,
+                    nh, block, pos0, pos_rows, ws, tickets, y, y_lo, C, err);
+  return launch_k(attn_decode_kernel<T, HSZ, PAGED, 4>, dim3(rows, splits), dim3(128), 0, st, false, q, kc, vc, kv, nh,
+                  block, pos0, pos_rows, ws, tickets, y, y_lo, C, err);
+}
+
 template <int EPI>
 cudaError_t launch_dl_epi(const CUtensorMap& tw, const CUtensorMap& tx, int kb, int splits, int stages, int n_tiles,
                           const Epi<bf16>& e, bool pdl, cudaStream_t st) {
@@ -999,22 +1013,19 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       const TE* qc = q;
       // Launched as an ordinary (not programmatic) dependent: its many small CTAs would otherwise
       // sit on the SMs the c_attn GEMM is still using (measured: 7 % slower decode steps at B=64).
+      const int* dpos = static_cast<const int*>(m->d_pos);
       if (m->hs == 64 && m->paged)
-        CK(launch_k(attn_decode_kernel<TE, 64, true>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
+        CK((launch_dec_attn<TE, 64, true>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
+                                          ch.tickets, y, y_lo, C, m->d_err)));
       else if (m->paged)
-        CK(launch_k(attn_decode_kernel<TE, 32, true>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
+        CK((launch_dec_attn<TE, 32, true>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
+                                          ch.tickets, y, y_lo, C, m->d_err)));
       else if (m->hs == 64)
-        CK(launch_k(attn_decode_kernel<TE, 64>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
+        CK((launch_dec_attn<TE, 64, false>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
+                                           ch.tickets, y, y_lo, C, m->d_err)));
       else
-        CK(launch_k(attn_decode_kernel<TE, 32>, dim3(B * nh, splits), dim3(DEC_THREADS), 0, st, false, qc,
-                    static_cast<const TE*>(kc), static_cast<const TE*>(vc), kvl, nh, m->block,
-                    static_cast<const int*>(m->d_pos), pos_rows, ch.ws, ch.tickets, y, y_lo, C, m->d_err));
+        CK((launch_dec_attn<TE, 32, false>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
+                                           ch.tickets, y, y_lo, C, m->d_err)));
     } else if constexpr (kBf16) {
       // q [B][nh][T][64] and this layer's cache rows as 2-D tensors for TMA
       const long long cache_rows = static_cast<long long>(m->cache_layer_bytes() / (m->hs * m->esz));
@@ -1378,6 +1389,35 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, int arrive, int* 
     if (arrive) mbar_arrive(&bar);
     mbar_wait_limit(&bar, 0, err, limit_ns);
   }
+}
+
+// The stand-alone decode attention (gpt_attention_decode and its no-allocation variant) on a
+// contiguous cache [B][n_head][block][head_size], with the caller's scratch.
+int launch_attn_decode_any(const void* q, const void* k_cache, const void* v_cache, int dtype, int B, int n_head,
+                           int head_size, int block, const int* pos0_dev, int splits, void* y, void* y_lo, float* ws,
+                           unsigned int* tickets, int* err, cudaStream_t st) {
+  const int C = head_size * n_head, rows = B * n_head;
+  const KvLayout kv{n_head, block};
+  cudaError_t e;
+  if (dtype == GPT_DTYPE_BF16) {
+    const bf16 *qq = static_cast<const bf16*>(q), *kk = static_cast<const bf16*>(k_cache),
+               *vv = static_cast<const bf16*>(v_cache);
+    bf16 *yy = static_cast<bf16*>(y), *yl = static_cast<bf16*>(y_lo);
+    e = head_size == 64 ? launch_dec_attn<bf16, 64, false>(rows, splits, st, qq, kk, vv, kv, n_head, block, pos0_dev,
+                                                           nullptr, ws, tickets, yy, yl, C, err)
+                        : launch_dec_attn<bf16, 32, false>(rows, splits, st, qq, kk, vv, kv, n_head, block, pos0_dev,
+                                                           nullptr, ws, tickets, yy, yl, C, err);
+  } else {
+    const float *qq = static_cast<const float*>(q), *kk = static_cast<const float*>(k_cache),
+                *vv = static_cast<const float*>(v_cache);
+    float* yy = static_cast<float*>(y);
+    e = head_size == 64 ? launch_dec_attn<float, 64, false>(rows, splits, st, qq, kk, vv, kv, n_head, block, pos0_dev,
+                                                            nullptr, ws, tickets, yy, nullptr, C, err)
+                        : launch_dec_attn<float, 32, false>(rows, splits, st, qq, kk, vv, kv, n_head, block, pos0_dev,
+                                                            nullptr, ws, tickets, yy, nullptr, C, err);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  return GPT_OK;
 }
 
 // Pointer alignment the stand-alone entry points check before any launch (their kernels use
@@ -1904,19 +1944,9 @@ int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache
   int rc = op_ctx(&c, pairs * splits * (head_size + 2) * sizeof(float), pairs);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int C = head_size * n_head;
-  const dim3 grid(B * n_head, splits);
-  if (dtype == GPT_DTYPE_BF16) {
-    auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
-    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
-                                       static_cast<const bf16*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
-                                       static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, c->err);
-  } else {
-    auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
-    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                       static_cast<const float*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, c->ws, c->tickets,
-                                       static_cast<float*>(y), nullptr, C, c->err);
-  }
+  rc = launch_attn_decode_any(q, k_cache, v_cache, dtype, B, n_head, head_size, block, pos0_dev, splits, y, y_lo,
+                              c->ws, c->tickets, c->err, st);
+  if (rc) return rc;
   CK(cudaGetLastError());
   return GPT_OK;
 }
@@ -2060,19 +2090,9 @@ int gpt_attention_decode_noalloc(const void* q, const void* k_cache, const void*
   int* err = err_dev ? err_dev : reinterpret_cast<int*>(base);
   // The array keeps whatever the previous call left: the merge tickets must start at zero.
   if (splits > 1) CK(cudaMemsetAsync(tickets, 0, pairs * sizeof(unsigned int), st));
-  const int C = head_size * n_head;
-  const dim3 grid(B * n_head, splits);
-  if (dtype == GPT_DTYPE_BF16) {
-    auto kern = head_size == 64 ? attn_decode_kernel<bf16, 64> : attn_decode_kernel<bf16, 32>;
-    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(k_cache),
-                                       static_cast<const bf16*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, ws, tickets,
-                                       static_cast<bf16*>(y), static_cast<bf16*>(y_lo), C, err);
-  } else {
-    auto kern = head_size == 64 ? attn_decode_kernel<float, 64> : attn_decode_kernel<float, 32>;
-    kern<<<grid, DEC_THREADS, 0, st>>>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                       static_cast<const float*>(v_cache), KvLayout{n_head, block}, n_head, block, pos0_dev, nullptr, ws, tickets,
-                                       static_cast<float*>(y), nullptr, C, err);
-  }
+  rc = launch_attn_decode_any(q, k_cache, v_cache, dtype, B, n_head, head_size, block, pos0_dev, splits, y, y_lo,
+                              ws, tickets, err, st);
+  if (rc) return rc;
   CK(cudaGetLastError());
   return GPT_OK;
 }
