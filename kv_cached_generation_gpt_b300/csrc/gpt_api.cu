@@ -1034,8 +1034,9 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       if (!rc) rc = m->weight_map(m->kcache(l), cache_rows, m->hs, PT_BK, &tk);
       if (!rc) rc = m->weight_map(m->vcache(l), cache_rows, m->hs, PT_BK, &tv);
       if (rc) return rc;
-      attn_prefill_tc<<<dim3(cdiv(T, PT_BQ), B * nh), PT_THREADS, PT_SMEM, st>>>(tq, tk, tv, kvl, nh, T, off, y, C,
-                                                                                m->d_err);
+      const int items = cdiv(T, PT_BQ) * B * nh;
+      attn_prefill_tc<<<std::min(items, PT_CTAS_PER_SM * m->num_sms), PT_THREADS, PT_SMEM, st>>>(
+          tq, tk, tv, kvl, nh, B * nh, T, off, y, C, m->d_err);
     } else {
       if (m->hs == 64)
         attn_prefill_f32<64><<<dim3(T, B * nh), 32, (off + T) * sizeof(float), st>>>(q, kc, vc, kvl, nh, T,
@@ -1914,8 +1915,12 @@ int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cach
     if ((rc = make_tmap(&tq, q, static_cast<long long>(B) * n_head * T, head_size, PT_BQ))) return rc;
     if ((rc = make_tmap(&tk, k_cache, rows, head_size, PT_BK))) return rc;
     if ((rc = make_tmap(&tv, v_cache, rows, head_size, PT_BK))) return rc;
-    attn_prefill_tc<<<dim3(cdiv(T, PT_BQ), B * n_head), PT_THREADS, PT_SMEM, st>>>(tq, tk, tv, kvl, n_head, T, pos0,
-                                                                                   static_cast<bf16*>(y), C, ctx->err);
+    int dev = 0, sms = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int items = cdiv(T, PT_BQ) * B * n_head;
+    attn_prefill_tc<<<std::min(items, PT_CTAS_PER_SM * sms), PT_THREADS, PT_SMEM, st>>>(
+        tq, tk, tv, kvl, n_head, B * n_head, T, pos0, static_cast<bf16*>(y), C, ctx->err);
   } else if (dtype == GPT_DTYPE_F32) {
     if ((pos0 + T) * sizeof(float) > 48 * 1024) return GPT_EINVAL;
     auto kern = head_size == 64 ? attn_prefill_f32<64> : attn_prefill_f32<32>;
