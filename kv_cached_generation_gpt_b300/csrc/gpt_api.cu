@@ -26,6 +26,7 @@
 
 #include "../../include/gpt.h"
 #include "attention.cuh"
+#include "attention_prefill.cuh"
 #include "common.cuh"
 #include "decode_linear.cuh"
 #include "gemm.cuh"
