@@ -140,10 +140,10 @@ __device__ __forceinline__ void dl_epilogue8(const Epi<__nv_bfloat16>& e, int r,
   }
 }
 
-// Bring the global operands of dl_epilogue8 for (row r, features n0..n0+7) into L1.
+// Bring the global operands of dl_epilogue8 for (row r, features n0..n0+7) that earlier kernels
+// write into L1 (the bias is fetched at the start).
 template <int EPI>
 __device__ __forceinline__ void dl_prefetch_epilogue(const Epi<__nv_bfloat16>& e, int r, int n0) {
-  if (e.bias) prefetch_l1(e.bias + n0);
   if (EPI == EPI_RESID) prefetch_l1(e.x + static_cast<size_t>(r) * e.ldx + n0);
   if (EPI == EPI_QKV && e.pos_rows) prefetch_l1(e.pos_rows + r);
 }
@@ -181,6 +181,10 @@ __global__ void __launch_bounds__(DL_THREADS) dec_linear_kernel(const __grid_con
   float* recv = reinterpret_cast<float*>(smem);  // [S][R][bp], over the ring
   uint32_t tcols = 32;
   while (tcols < static_cast<uint32_t>(2 * bp)) tcols <<= 1;
+
+  // the bias of this CTA's R features does not depend on earlier kernels: into L1 now
+  if (e.bias && threadIdx.x * 32 < R && tile * 128 + rank * R + static_cast<int>(threadIdx.x) * 32 < e.N)
+    prefetch_l1(e.bias + tile * 128 + rank * R + threadIdx.x * 32);
 
   auto w_tile = [&](int s) { return smem + s * stage_bytes; };
   auto x_tile = [&](int s) { return smem + s * stage_bytes + DL_W_BYTES; };

@@ -528,9 +528,15 @@ cudaError_t launch_ln(int rows, int C, long long in_stride, const float* x, cons
                       TO* y, TO* y_lo, int ldy, cudaStream_t st, bool pdl) {
   const dim3 grid(cdiv(rows, 8)), block(256);
   if (C <= 12 * 64)
-    return launch_k(layernorm_kernel<TO, 12>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta, y, y_lo, ldy);
+    return pdl ? launch_k(layernorm_kernel<TO, 12, true>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta,
+                          y, y_lo, ldy)
+               : launch_k(layernorm_kernel<TO, 12, false>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma,
+                          beta, y, y_lo, ldy);
   if (C <= 16 * 64)
-    return launch_k(layernorm_kernel<TO, 16>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta, y, y_lo, ldy);
+    return pdl ? launch_k(layernorm_kernel<TO, 16, true>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta,
+                          y, y_lo, ldy)
+               : launch_k(layernorm_kernel<TO, 16, false>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma,
+                          beta, y, y_lo, ldy);
   return launch_k(layernorm_kernel<TO, LN_MAX_PAIRS>, grid, block, 0, st, pdl, x, rows, C, in_stride, gamma, beta, y,
                   y_lo, ldy);
 }

@@ -59,17 +59,29 @@ __device__ __forceinline__ void store_pair(__nv_bfloat16* p, float a, float b) {
 // y[r, :] = LN(x[r * in_stride + :]) for r < rows; warp per row.  TO is bf16 or f32.
 // With y_lo, also writes the rounding remainder y - bf16(y) (the lo half of a hi/lo pair).
 // MAXP bounds C / 64 (the float pairs a lane holds), so small models keep few registers.
-template <typename TO, int MAXP = LN_MAX_PAIRS>
+// EARLY (programmatic dependent launches of a decode step, a few rows): gamma and beta, which
+// do not depend on earlier kernels, are fetched into registers before waiting for them; the
+// many-row prefill form loads them at use and keeps its registers (and occupancy).
+template <typename TO, int MAXP = LN_MAX_PAIRS, bool EARLY = false>
 __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, long long in_stride,
                                  const float* __restrict__ gamma, const float* __restrict__ beta,
                                  TO* __restrict__ y, TO* __restrict__ y_lo, int ldy) {
+  const int lane = threadIdx.x & 31;
+  const int np = C / 64;
+  float2 g2[MAXP], b2[MAXP];
+#pragma unroll
+  for (int i = 0; i < MAXP; ++i) {
+    if (EARLY && i < np) {
+      const int c = i * 64 + lane * 2;
+      g2[i] = *reinterpret_cast<const float2*>(gamma + c);
+      b2[i] = beta ? *reinterpret_cast<const float2*>(beta + c) : make_float2(0.0f, 0.0f);
+    }
+  }
   griddep_wait();  // x comes from the previous kernel (a programmatic dependent launch may start early)
   griddep_launch();
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
   if (r >= rows) return;
   const float* xr = x + static_cast<size_t>(r) * in_stride;
-  const int np = C / 64;
   float2 v[MAXP];
   float s = 0.0f;
 #pragma unroll
@@ -95,13 +107,15 @@ __global__ void layernorm_kernel(const float* __restrict__ x, int rows, int C, l
   for (int i = 0; i < MAXP; ++i) {
     if (i < np) {
       const int c = i * 64 + lane * 2;
-      const float2 g2 = *reinterpret_cast<const float2*>(gamma + c);
-      float a = (v[i].x - mean) * rstd * g2.x;
-      float b = (v[i].y - mean) * rstd * g2.y;
+      if (!EARLY) {
+        g2[i] = *reinterpret_cast<const float2*>(gamma + c);
+        if (beta) b2[i] = *reinterpret_cast<const float2*>(beta + c);
+      }
+      float a = (v[i].x - mean) * rstd * g2[i].x;
+      float b = (v[i].y - mean) * rstd * g2[i].y;
       if (beta) {
-        const float2 b2 = *reinterpret_cast<const float2*>(beta + c);
-        a += b2.x;
-        b += b2.y;
+        a += b2[i].x;
+        b += b2[i].y;
       }
       store_pair(yr + c, a, b);
       if (y_lo) {

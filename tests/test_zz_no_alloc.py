@@ -75,3 +75,36 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     # 64 x 12 pairs x 32 splits x 66 floats = 6.5 MB of partials > 4 MiB
     assert lib.gpt_attention_decode_noalloc(p, p, p, 1, 64, 12, 64, 1024, p, 32, p, None, None, None) == G.GPT_ETOOBIG
     assert "max" in lib.gpt_last_error_detail().decode()
+
+
+def test_noalloc_captured_in_a_graph_and_replayed_between_eager_calls():
+    """The shared ticket area sees eager calls and graph replays of the same entry point in
+    turn, with split-KV merges in both; each result must equal the allocating entry point's."""
+    B, nh, hs, block, t, splits = 3, 4, 64, 256, 200, 5
+    dt = torch.bfloat16
+    q, kc, vc, pos0 = _inputs(7, B, nh, hs, block, t, dt)
+    y_ref = torch.empty(B, nh * hs, device="cuda", dtype=dt)
+    lo_ref = torch.empty_like(y_ref)
+    G.gpt_attention_decode(q, kc, vc, pos0, splits, y_ref, lo_ref)
+    ref = y_ref.float().cpu().numpy().astype(np.float64) + lo_ref.float().cpu().numpy()
+    y = torch.zeros_like(y_ref)
+    lo = torch.zeros_like(y_ref)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.gpt_attention_decode_noalloc(q, kc, vc, pos0, splits, y, lo, err)  # first call: the address is cached
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        G.gpt_attention_decode_noalloc(q, kc, vc, pos0, splits, y, lo, err)
+    for _ in range(2):
+        for replay in (False, True):
+            y.zero_()
+            lo.zero_()
+            if replay:
+                graph.replay()
+            else:
+                G.gpt_attention_decode_noalloc(q, kc, vc, pos0, splits, y, lo, err)
+            torch.cuda.synchronize()
+            assert G.gpt_op_status() == G.GPT_OK
+            assert int(err.item()) == 0
+            got = y.float().cpu().numpy().astype(np.float64) + lo.float().cpu().numpy()
+            assert np.max(np.abs(got - ref)) < 2e-5, replay
