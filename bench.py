@@ -545,7 +545,8 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded random-init GPT-2 124M weights in bf16, uniform token ids)",
         "config": workload_config(wl),
-        "roofline": {"bound": "hbm", "kernel": f"attn_decode_kernel<bf16,64> at {half} sequences (one decode chain)",
+        "roofline": {"bound": "hbm",
+                     "kernel": f"attn_decode_bulk<bf16,64> at {half} sequences (one decode chain), launched alone",
                      "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": attn_traffic_per_launch(),
                      "algorithmic_bytes_per_launch": bytes_per_launch, "peak_source": pk_kind,

@@ -12,6 +12,10 @@
 //   attn_decode_kernel  -- one new query per (b, h); split-KV over the keys, 8 lanes per key
 //                          with 128-bit loads, warp-shuffle reductions, online softmax in
 //                          fp32, splits merged by log-sum-exp in a fixed order.
+//   attn_decode_bulk    -- the same for bf16 / head size 64 / one split per (b, h) (grids of up
+//                          to 512 CTAs), the cache rows streamed through a shared-memory ring by
+//                          bulk copies; in a decode step it starts on the older rows before the
+//                          kernel that appends the newest key has finished.
 //   attn_prefill_tc     -- (attention_prefill.cuh) FlashAttention-style tiles on tcgen05.
 //   attn_prefill_f32    -- exact fp32 path for fp32 models (warp per query).
 #pragma once
@@ -242,6 +246,192 @@ __global__ void __launch_bounds__(32 * DEC_WARPS) attn_decode_kernel(const T* __
     if (y_lo) y_lo[yoff + d] = from_f32<T>(o - to_f32(ho));
   }
   if (threadIdx.x == 0) tickets[bh] = 0u;
+}
+
+// ------------------------------------------------------------------ decode, streamed through shared memory
+
+// The same decode attention for bf16, head size 64 and one split per (b, h), with the cache
+// rows streamed through shared memory instead of registers: a producer warp issues untiled bulk
+// copies of DB_KEYS consecutive K rows and the matching V rows (2 x 8 KiB) into a ring of
+// DB_STAGES stages, and 8 consumer warps score and accumulate from shared memory.  A CTA then
+// keeps up to 48 KiB of loads in flight however few registers its warps hold, which is what a
+// grid of a few hundred CTAs (one 32-sequence decode chain) lacks with register loads; 48 KiB
+// (not more) so that four CTAs fit an SM beside the kernels of the other decode chain.
+// Measured on the B=64 decode step (two chains of 32 sequences): 3 stages of 64 keys 658 us per
+// step, against 689 (4 x 64), 661 (2 x 96), 725 (2 x 64), 737-741 (3-4 x 32) and 720 us for the
+// register-load kernel.
+// Key j of a stage goes to warp (j mod 32) / 4, lane group j mod 4, as in attn_decode_kernel;
+// the online softmax is rescaled once per stage.  A stage of 64 keys starts at a multiple of 64,
+// so with a paged cache (pages of at least 64 positions, a power of two) it lies in one page.
+constexpr int DB_WARPS = 8;                           // consumer warps
+constexpr int DB_THREADS = 32 * (DB_WARPS + 1);       // + the producer warp
+constexpr int DB_KEYS = 64;                           // keys per stage
+constexpr int DB_STAGES = 3;
+constexpr uint32_t DB_ROW_BYTES = HS * 2;             // one bf16 cache row
+constexpr uint32_t DB_STAGE_BYTES = 2 * DB_KEYS * DB_ROW_BYTES;  // K rows, then V rows
+constexpr uint32_t DB_SMEM = DB_STAGES * DB_STAGE_BYTES + 2 * DB_STAGES * 8;
+
+// grid (B*nh): keys 0..t_len-1, t_len = *pos0 + 1 (or pos_rows[b] + 1); y [B][C] (+ y_lo).
+// EARLY (a decode step's programmatic dependent launch): the cache length and every row before
+// the newest key were written before the step began, so the producer reads the length and fills
+// the ring with those rows before waiting for the kernel that appends the newest key; q and
+// the chunk holding that key wait for it.
+template <bool PAGED, bool EARLY = false>
+__global__ void __launch_bounds__(DB_THREADS) attn_decode_bulk(const __nv_bfloat16* __restrict__ q,
+                                                                const __nv_bfloat16* __restrict__ kc,
+                                                                const __nv_bfloat16* __restrict__ vc, KvLayout kv,
+                                                                int nh, int block, const int* pos0,
+                                                                const int* pos_rows, __nv_bfloat16* __restrict__ y,
+                                                                __nv_bfloat16* __restrict__ y_lo, int C, int* err) {
+  extern __shared__ __align__(128) uint8_t db_smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(db_smem + DB_STAGES * DB_STAGE_BYTES);
+  uint64_t* empty = full + DB_STAGES;
+  __shared__ float s_m[DB_WARPS], s_l[DB_WARPS];
+  __shared__ float s_acc[DB_WARPS][HS];
+  const int bh = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = lane & 7, g = lane >> 3;  // 8 lanes per key, 4 keys per warp per pass
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < DB_STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], DB_WARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool producer = warp == DB_WARPS;
+  if (!(EARLY && producer)) griddep_wait();  // q and the new key/value come from the previous kernel
+  griddep_launch();
+  const int t_len = (pos_rows ? pos_rows[bh / nh] : *pos0) + 1;
+  if (t_len > block) {
+    if (threadIdx.x == 0) atomicOr(err, ERR_POSITION);
+    return;
+  }
+  const int bq = bh / nh, hq = bh - bq * nh;
+  const int nchunks = (t_len + DB_KEYS - 1) / DB_KEYS;
+
+  if (producer) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // every cache row is read once per step
+      const size_t row0 = PAGED ? 0 : (static_cast<size_t>(bq) * kv.nh + hq) * kv.block;
+      // chunks wholly before the newest key (t_len - 1) need not wait for the previous kernel
+      const int ready = EARLY ? (t_len - 1) / DB_KEYS : 0;
+      int c = 0;
+      for (; c < nchunks; ++c) {
+        const int st = c % DB_STAGES;
+        if (EARLY && c == min(ready, DB_STAGES)) griddep_wait();
+        if (c >= DB_STAGES && !mbar_wait(&empty[st], ((c / DB_STAGES) & 1) ^ 1, err)) break;
+        const int k0 = c * DB_KEYS;
+        const uint32_t bytes = static_cast<uint32_t>(min(DB_KEYS, t_len - k0)) * DB_ROW_BYTES;
+        const size_t row = PAGED ? kv.row(bq, hq, k0) : row0 + k0;
+        uint8_t* dst = db_smem + st * DB_STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[st], 2 * bytes);
+        bulk_load(dst, kc + row * HS, bytes, &full[st], pol);
+        bulk_load(dst + DB_KEYS * DB_ROW_BYTES, vc + row * HS, bytes, &full[st], pol);
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int t = max(0, c - DB_STAGES); t < c; ++t) mbar_wait(&full[t % DB_STAGES], (t / DB_STAGES) & 1, err);
+    }
+    return;  // the producer warp takes no part in the merge below (named barrier of the consumers)
+  }
+
+  float qv[8];
+  {
+    Vec8<__nv_bfloat16> t;
+    t.load(q + static_cast<size_t>(bh) * HS + e * 8);
+    t.to_float(qv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qv[i] *= 0.125f * LOG2E_F;  // 1/sqrt(64), log2 units
+  }
+  float m = -INFINITY, l = 0.0f, acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  constexpr int U = DB_KEYS / 32;  // keys per lane group per stage
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c % DB_STAGES;
+    if (!mbar_wait(&full[st], (c / DB_STAGES) & 1, err)) break;
+    const uint32_t sk = smem_u32(db_smem + st * DB_STAGE_BYTES), sv = sk + DB_KEYS * DB_ROW_BYTES;
+    const int k0 = c * DB_KEYS;
+    float sc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int kk = u * 32 + warp * 4 + g;
+      float d = 0.0f;
+      if (k0 + kk < t_len) {
+        Vec8<__nv_bfloat16> kr;
+        kr.u = ld_shared_u4(sk + kk * DB_ROW_BYTES + e * 16);
+        float kf[8];
+        kr.to_float(kf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d = fmaf(qv[i], kf[i], d);
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      sc[u] = (k0 + kk < t_len) ? d : -INFINITY;
+    }
+    float mn = m;
+#pragma unroll
+    for (int u = 0; u < U; ++u) mn = fmaxf(mn, sc[u]);
+    const float corr = (mn == -INFINITY) ? 1.0f : exp2f(m - mn);
+    l *= corr;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= corr;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int kk = u * 32 + warp * 4 + g;
+      if (k0 + kk < t_len) {
+        const float p = exp2f(sc[u] - mn);
+        l += p;
+        Vec8<__nv_bfloat16> vr;
+        vr.u = ld_shared_u4(sv + kk * DB_ROW_BYTES + e * 16);
+        float vf[8];
+        vr.to_float(vf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
+      }
+    }
+    m = mn;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+  }
+
+  // merge the 4 lane groups of the warp, then the 8 warps (as attn_decode_kernel)
+#pragma unroll
+  for (int o = 8; o <= 16; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    const float mn = fmaxf(m, m2);
+    const float c1 = (m == -INFINITY) ? 0.0f : exp2f(m - mn);
+    const float c2 = (m2 == -INFINITY) ? 0.0f : exp2f(m2 - mn);
+    l = l * c1 + l2 * c2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = acc[i] * c1 + __shfl_xor_sync(0xffffffffu, acc[i], o) * c2;
+    m = mn;
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s_acc[warp][e * 8 + i] = acc[i];
+    if (e == 0) {
+      s_m[warp] = m;
+      s_l[warp] = l;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * DB_WARPS) : "memory");
+  const int d = threadIdx.x;
+  if (d < HS) {
+    float M = -INFINITY, L = 0.0f, A = 0.0f;
+    for (int w = 0; w < DB_WARPS; ++w) M = fmaxf(M, s_m[w]);
+    for (int w = 0; w < DB_WARPS; ++w) {
+      const float cw = (s_m[w] == -INFINITY) ? 0.0f : exp2f(s_m[w] - M);
+      L += s_l[w] * cw;
+      A += s_acc[w][d] * cw;
+    }
+    const size_t yoff = static_cast<size_t>(bq) * C + hq * HS;
+    const float o = A / L;
+    const __nv_bfloat16 ho = __float2bfloat16_rn(o);
+    y[yoff + d] = ho;
+    if (y_lo) y_lo[yoff + d] = __float2bfloat16_rn(o - __bfloat162float(ho));
+  }
 }
 
 // ------------------------------------------------------------------ prefill, fp32

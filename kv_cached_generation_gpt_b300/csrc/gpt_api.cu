@@ -409,10 +409,42 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // Decode attention over a grid of (rows x splits) CTAs: the 8-warp form for small grids, the
 // 4-warp form otherwise (DEC_WIDE_MAX_CTAS).  The choice depends on the shapes only, so every
 // entry point gives the same results for the same inputs.
+unsigned long long g_db_attr_mask[2] = {};  // per paged flag: devices whose smem attribute is set
+std::mutex g_db_mu;
+
+template <bool PAGED>
+cudaError_t db_attr(int dev) {
+  std::lock_guard<std::mutex> lk(g_db_mu);
+  if (g_db_attr_mask[PAGED] & (1ull << dev)) return cudaSuccess;
+  cudaError_t r = cudaFuncSetAttribute(attn_decode_bulk<PAGED, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(DB_SMEM));
+  if (r == cudaSuccess)
+    r = cudaFuncSetAttribute(attn_decode_bulk<PAGED, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(DB_SMEM));
+  if (r == cudaSuccess) g_db_attr_mask[PAGED] |= 1ull << dev;
+  return r;
+}
+
 template <typename T, int HSZ, bool PAGED>
 cudaError_t launch_dec_attn(int rows, int splits, cudaStream_t st, const T* q, const T* kc, const T* vc,
                             const KvLayout& kv, int nh, int block, const int* pos0, const int* pos_rows, float* ws,
-                            unsigned int* tickets, T* y, T* y_lo, int C, int* err) {
+                            unsigned int* tickets, T* y, T* y_lo, int C, int* err, bool step = false) {
+  if constexpr (std::is_same<T, bf16>::value && HSZ == 64) {
+    // one split per (b, h): the cache rows streamed through shared memory; within a decode step
+    // (step) as a programmatic dependent that streams the older rows before the c_attn kernel
+    // that appends the newest one has finished
+    if (splits == 1 && rows <= DEC_WIDE_MAX_CTAS) {
+      int dev = 0;
+      cudaError_t r = cudaGetDevice(&dev);
+      if (r == cudaSuccess) r = db_attr<PAGED>(dev);
+      if (r != cudaSuccess) return r;
+      if (step)
+        return launch_k(attn_decode_bulk<PAGED, true>, dim3(rows), dim3(DB_THREADS), DB_SMEM, st, true, q, kc, vc,
+                        kv, nh, block, pos0, pos_rows, y, y_lo, C, err);
+      return launch_k(attn_decode_bulk<PAGED, false>, dim3(rows), dim3(DB_THREADS), DB_SMEM, st, false, q, kc, vc, kv,
+                      nh, block, pos0, pos_rows, y, y_lo, C, err);
+    }
+  }
   if (static_cast<long long>(rows) * splits <= DEC_WIDE_MAX_CTAS)
     return launch_k(attn_decode_kernel<T, HSZ, PAGED, 8>, dim3(rows, splits), dim3(256), 0, st, false, q, kc, vc, kv,
                     nh, block, pos0, pos_rows, ws, tickets, y, y_lo, C, err);
@@ -1023,16 +1055,16 @@ int enqueue_forward(gpt_model* m, const int* tokens, int B, int T, bool decode, 
       const int* dpos = static_cast<const int*>(m->d_pos);
       if (m->hs == 64 && m->paged)
         CK((launch_dec_attn<TE, 64, true>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
-                                          ch.tickets, y, y_lo, C, m->d_err)));
+                                          ch.tickets, y, y_lo, C, m->d_err, true)));
       else if (m->paged)
         CK((launch_dec_attn<TE, 32, true>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
-                                          ch.tickets, y, y_lo, C, m->d_err)));
+                                          ch.tickets, y, y_lo, C, m->d_err, true)));
       else if (m->hs == 64)
         CK((launch_dec_attn<TE, 64, false>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
-                                           ch.tickets, y, y_lo, C, m->d_err)));
+                                           ch.tickets, y, y_lo, C, m->d_err, true)));
       else
         CK((launch_dec_attn<TE, 32, false>(B * nh, splits, st, qc, kc, vc, kvl, nh, m->block, dpos, pos_rows, ch.ws,
-                                           ch.tickets, y, y_lo, C, m->d_err)));
+                                           ch.tickets, y, y_lo, C, m->d_err, true)));
     } else if constexpr (kBf16) {
       // q [B][nh][T][64] and this layer's cache rows as 2-D tensors for TMA
       const long long cache_rows = static_cast<long long>(m->cache_layer_bytes() / (m->hs * m->esz));
