@@ -12,10 +12,10 @@
 //   attn_decode_kernel  -- one new query per (b, h); split-KV over the keys, 8 lanes per key
 //                          with 128-bit loads, warp-shuffle reductions, online softmax in
 //                          fp32, splits merged by log-sum-exp in a fixed order.
-//   attn_decode_bulk    -- the same for bf16 / head size 64 / one split per (b, h) (grids of up
-//                          to 512 CTAs), the cache rows streamed through a shared-memory ring by
-//                          bulk copies; in a decode step it starts on the older rows before the
-//                          kernel that appends the newest key has finished.
+//   attn_decode_bulk    -- the same for bf16 / head size 64 / up to DB_MAX_SPLITS splits per
+//                          (b, h) (at most 512 (b, h) pairs), the cache rows streamed through a
+//                          shared-memory ring by bulk copies; in a decode step it starts on the
+//                          older rows before the kernel that appends the newest key has finished.
 //   attn_prefill_tc     -- (attention_prefill.cuh) FlashAttention-style tiles on tcgen05.
 //   attn_prefill_f32    -- exact fp32 path for fp32 models (warp per query).
 #pragma once
@@ -267,11 +267,15 @@ constexpr int DB_WARPS = 8;                           // consumer warps
 constexpr int DB_THREADS = 32 * (DB_WARPS + 1);       // + the producer warp
 constexpr int DB_KEYS = 64;                           // keys per stage
 constexpr int DB_STAGES = 3;
+constexpr int DB_MAX_SPLITS = 8;                      // splits per (b, h), whole stages each
 constexpr uint32_t DB_ROW_BYTES = HS * 2;             // one bf16 cache row
 constexpr uint32_t DB_STAGE_BYTES = 2 * DB_KEYS * DB_ROW_BYTES;  // K rows, then V rows
 constexpr uint32_t DB_SMEM = DB_STAGES * DB_STAGE_BYTES + 2 * DB_STAGES * 8;
 
-// grid (B*nh): keys 0..t_len-1, t_len = *pos0 + 1 (or pos_rows[b] + 1); y [B][C] (+ y_lo).
+// grid (B*nh, splits): keys 0..t_len-1, t_len = *pos0 + 1 (or pos_rows[b] + 1), in stages of
+// DB_KEYS; split s takes stages [s*cps, (s+1)*cps), cps = ceil(stages / splits), and with
+// splits > 1 leaves (m, l, acc[64]) in ws for the last split to finish (ticket) to merge in
+// split order, as attn_decode_kernel does.  y [B][C] (+ y_lo).
 // EARLY (a decode step's programmatic dependent launch): the cache length and every row before
 // the newest key were written before the step began, so the producer reads the length and fills
 // the ring with those rows before waiting for the kernel that appends the newest key; q and
@@ -281,14 +285,17 @@ __global__ void __launch_bounds__(DB_THREADS) attn_decode_bulk(const __nv_bfloat
                                                                 const __nv_bfloat16* __restrict__ kc,
                                                                 const __nv_bfloat16* __restrict__ vc, KvLayout kv,
                                                                 int nh, int block, const int* pos0,
-                                                                const int* pos_rows, __nv_bfloat16* __restrict__ y,
+                                                                const int* pos_rows, float* __restrict__ ws,
+                                                                unsigned int* __restrict__ tickets,
+                                                                __nv_bfloat16* __restrict__ y,
                                                                 __nv_bfloat16* __restrict__ y_lo, int C, int* err) {
   extern __shared__ __align__(128) uint8_t db_smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(db_smem + DB_STAGES * DB_STAGE_BYTES);
   uint64_t* empty = full + DB_STAGES;
   __shared__ float s_m[DB_WARPS], s_l[DB_WARPS];
   __shared__ float s_acc[DB_WARPS][HS];
-  const int bh = blockIdx.x;
+  __shared__ int s_last;
+  const int bh = blockIdx.x, split = blockIdx.y, splits = gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = lane & 7, g = lane >> 3;  // 8 lanes per key, 4 keys per warp per pass
   if (threadIdx.x == 0) {
@@ -308,20 +315,23 @@ __global__ void __launch_bounds__(DB_THREADS) attn_decode_bulk(const __nv_bfloat
     return;
   }
   const int bq = bh / nh, hq = bh - bq * nh;
-  const int nchunks = (t_len + DB_KEYS - 1) / DB_KEYS;
+  const int n_all = (t_len + DB_KEYS - 1) / DB_KEYS;  // stages of the whole (b, h)
+  const int cps = (n_all + splits - 1) / splits;
+  const int c_beg = min(split * cps, n_all);
+  const int nchunks = min(c_beg + cps, n_all) - c_beg;  // this split's stages (possibly none)
 
   if (producer) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();  // every cache row is read once per step
       const size_t row0 = PAGED ? 0 : (static_cast<size_t>(bq) * kv.nh + hq) * kv.block;
-      // chunks wholly before the newest key (t_len - 1) need not wait for the previous kernel
-      const int ready = EARLY ? (t_len - 1) / DB_KEYS : 0;
+      // stages wholly before the newest key (t_len - 1) need not wait for the previous kernel
+      const int ready = EARLY ? min(max((t_len - 1) / DB_KEYS - c_beg, 0), nchunks) : 0;
       int c = 0;
       for (; c < nchunks; ++c) {
         const int st = c % DB_STAGES;
         if (EARLY && c == min(ready, DB_STAGES)) griddep_wait();
         if (c >= DB_STAGES && !mbar_wait(&empty[st], ((c / DB_STAGES) & 1) ^ 1, err)) break;
-        const int k0 = c * DB_KEYS;
+        const int k0 = (c_beg + c) * DB_KEYS;
         const uint32_t bytes = static_cast<uint32_t>(min(DB_KEYS, t_len - k0)) * DB_ROW_BYTES;
         const size_t row = PAGED ? kv.row(bq, hq, k0) : row0 + k0;
         uint8_t* dst = db_smem + st * DB_STAGE_BYTES;
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(DB_THREADS) attn_decode_bulk(const __nv_bfloat
     const int st = c % DB_STAGES;
     if (!mbar_wait(&full[st], (c / DB_STAGES) & 1, err)) break;
     const uint32_t sk = smem_u32(db_smem + st * DB_STAGE_BYTES), sv = sk + DB_KEYS * DB_ROW_BYTES;
-    const int k0 = c * DB_KEYS;
+    const int k0 = (c_beg + c) * DB_KEYS;
     float sc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -418,20 +428,55 @@ __global__ void __launch_bounds__(DB_THREADS) attn_decode_bulk(const __nv_bfloat
   }
   asm volatile("bar.sync 1, %0;" ::"r"(32 * DB_WARPS) : "memory");
   const int d = threadIdx.x;
+  float M = -INFINITY, L = 0.0f, A = 0.0f;
   if (d < HS) {
-    float M = -INFINITY, L = 0.0f, A = 0.0f;
     for (int w = 0; w < DB_WARPS; ++w) M = fmaxf(M, s_m[w]);
     for (int w = 0; w < DB_WARPS; ++w) {
       const float cw = (s_m[w] == -INFINITY) ? 0.0f : exp2f(s_m[w] - M);
       L += s_l[w] * cw;
       A += s_acc[w][d] * cw;
     }
-    const size_t yoff = static_cast<size_t>(bq) * C + hq * HS;
-    const float o = A / L;
+  }
+  const size_t yoff = static_cast<size_t>(bq) * C + hq * HS;
+  if (splits == 1) {
+    if (d < HS) {
+      const float o = A / L;
+      const __nv_bfloat16 ho = __float2bfloat16_rn(o);
+      y[yoff + d] = ho;
+      if (y_lo) y_lo[yoff + d] = __float2bfloat16_rn(o - __bfloat162float(ho));
+    }
+    return;
+  }
+  // splits: partial (m, l, acc) to ws; the last split of the (b, h) to take the ticket merges
+  float* part = ws + (static_cast<size_t>(bh) * splits + split) * (HS + 2);
+  if (d < HS) part[2 + d] = A;
+  if (d == 0) {
+    part[0] = M;
+    part[1] = L;
+  }
+  __threadfence();
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * DB_WARPS) : "memory");
+  if (threadIdx.x == 0) s_last = atomicAdd(&tickets[bh], 1u) == static_cast<unsigned>(splits - 1);
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * DB_WARPS) : "memory");
+  if (!s_last) return;
+  __threadfence();
+  if (d < HS) {
+    float MM = -INFINITY;
+    for (int sp = 0; sp < splits; ++sp) MM = fmaxf(MM, __ldcg(ws + (static_cast<size_t>(bh) * splits + sp) * (HS + 2)));
+    float LL = 0.0f, AA = 0.0f;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float* p = ws + (static_cast<size_t>(bh) * splits + sp) * (HS + 2);
+      const float ms = __ldcg(p);
+      const float cw = (ms == -INFINITY) ? 0.0f : exp2f(ms - MM);
+      LL += __ldcg(p + 1) * cw;
+      AA += __ldcg(p + 2 + d) * cw;
+    }
+    const float o = AA / LL;
     const __nv_bfloat16 ho = __float2bfloat16_rn(o);
     y[yoff + d] = ho;
     if (y_lo) y_lo[yoff + d] = __float2bfloat16_rn(o - __bfloat162float(ho));
   }
+  if (threadIdx.x == 0) tickets[bh] = 0u;
 }
 
 // ------------------------------------------------------------------ prefill, fp32

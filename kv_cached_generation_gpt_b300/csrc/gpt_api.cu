@@ -430,19 +430,19 @@ cudaError_t launch_dec_attn(int rows, int splits, cudaStream_t st, const T* q, c
                             const KvLayout& kv, int nh, int block, const int* pos0, const int* pos_rows, float* ws,
                             unsigned int* tickets, T* y, T* y_lo, int C, int* err, bool step = false) {
   if constexpr (std::is_same<T, bf16>::value && HSZ == 64) {
-    // one split per (b, h): the cache rows streamed through shared memory; within a decode step
-    // (step) as a programmatic dependent that streams the older rows before the c_attn kernel
-    // that appends the newest one has finished
-    if (splits == 1 && rows <= DEC_WIDE_MAX_CTAS) {
+    // up to DB_MAX_SPLITS splits per (b, h): the cache rows streamed through shared memory;
+    // within a decode step (step) as a programmatic dependent that streams the older rows before
+    // the c_attn kernel that appends the newest one has finished
+    if (splits <= DB_MAX_SPLITS && rows <= DEC_WIDE_MAX_CTAS) {
       int dev = 0;
       cudaError_t r = cudaGetDevice(&dev);
       if (r == cudaSuccess) r = db_attr<PAGED>(dev);
       if (r != cudaSuccess) return r;
       if (step)
-        return launch_k(attn_decode_bulk<PAGED, true>, dim3(rows), dim3(DB_THREADS), DB_SMEM, st, true, q, kc, vc,
-                        kv, nh, block, pos0, pos_rows, y, y_lo, C, err);
-      return launch_k(attn_decode_bulk<PAGED, false>, dim3(rows), dim3(DB_THREADS), DB_SMEM, st, false, q, kc, vc, kv,
-                      nh, block, pos0, pos_rows, y, y_lo, C, err);
+        return launch_k(attn_decode_bulk<PAGED, true>, dim3(rows, splits), dim3(DB_THREADS), DB_SMEM, st, true, q, kc,
+                        vc, kv, nh, block, pos0, pos_rows, ws, tickets, y, y_lo, C, err);
+      return launch_k(attn_decode_bulk<PAGED, false>, dim3(rows, splits), dim3(DB_THREADS), DB_SMEM, st, false, q, kc,
+                      vc, kv, nh, block, pos0, pos_rows, ws, tickets, y, y_lo, C, err);
     }
   }
   if (static_cast<long long>(rows) * splits <= DEC_WIDE_MAX_CTAS)
@@ -930,6 +930,10 @@ int decode_attn_splits(const gpt_model* m, int B, size_t ws_bytes, size_t n_tick
   const int pairs = B * m->nh;
   int s = cdiv(2 * m->num_sms, pairs);
   s = std::max(1, std::min(s, std::min(32, cdiv(m->block, 16))));
+  // the streamed kernel (bf16, head size 64, at most 512 pairs): about one CTA per SM, whole
+  // stages of 64 keys per split
+  if (m->bf16 && m->hs == 64 && pairs <= DEC_WIDE_MAX_CTAS)
+    s = std::max(1, std::min(std::min(DB_MAX_SPLITS, cdiv(m->num_sms, pairs)), cdiv(m->block, DB_KEYS)));
   while (s > 1 && static_cast<size_t>(pairs) * s * (m->hs + 2) * sizeof(float) > ws_bytes) --s;
   if (static_cast<size_t>(pairs) > n_tickets) s = 1;
   return s;
