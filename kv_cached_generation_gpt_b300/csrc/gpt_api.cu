@@ -930,10 +930,11 @@ int decode_attn_splits(const gpt_model* m, int B, size_t ws_bytes, size_t n_tick
   const int pairs = B * m->nh;
   int s = cdiv(2 * m->num_sms, pairs);
   s = std::max(1, std::min(s, std::min(32, cdiv(m->block, 16))));
-  // the streamed kernel (bf16, head size 64, at most 512 pairs): about one CTA per SM, whole
-  // stages of 64 keys per split
+  // the streamed kernel (bf16, head size 64, at most 512 pairs): the same target of about two
+  // CTAs per SM, at most DB_MAX_SPLITS splits of whole 64-key stages (one CTA per SM was
+  // slower at 128 pairs, the 350M shape at B=8: 1058 against 1022 us per step)
   if (m->bf16 && m->hs == 64 && pairs <= DEC_WIDE_MAX_CTAS)
-    s = std::max(1, std::min(std::min(DB_MAX_SPLITS, cdiv(m->num_sms, pairs)), cdiv(m->block, DB_KEYS)));
+    s = std::max(1, std::min(std::min(DB_MAX_SPLITS, cdiv(2 * m->num_sms, pairs)), cdiv(m->block, DB_KEYS)));
   while (s > 1 && static_cast<size_t>(pairs) * s * (m->hs + 2) * sizeof(float) > ws_bytes) --s;
   if (static_cast<size_t>(pairs) > n_tickets) s = 1;
   return s;

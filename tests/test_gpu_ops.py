@@ -300,7 +300,8 @@ def test_attention_prefill_matches_oracle(dt, hs, B, nh, T, pos0, block):
 @pytest.mark.parametrize("dt,hs", [(torch.bfloat16, 64), (torch.float32, 64), (torch.float32, 32),
                                    (torch.bfloat16, 32)])
 @pytest.mark.parametrize("B,nh,t,splits,block", [(1, 1, 1, 1, 8), (1, 12, 129, 8, 1024), (3, 2, 1024, 1, 1024),
-                                                 (2, 4, 77, 3, 96), (64, 12, 600, 1, 1024), (1, 12, 1000, 32, 1024)])
+                                                 (2, 4, 77, 3, 96), (64, 12, 600, 1, 1024), (1, 12, 1000, 32, 1024),
+                                                 (4, 12, 128, 2, 256), (2, 3, 64, 4, 64), (32, 12, 65, 1, 128)])
 def test_attention_decode_matches_oracle(dt, hs, B, nh, t, splits, block):
     r = _rng(B + nh * 10 + t)
     q = torch.from_numpy(r.standard_normal((B, nh, 1, hs)).astype(np.float32)).to(dt).cuda()
