@@ -282,9 +282,10 @@ int gpt_attention_prefill(const void* q, const void* k_cache, const void* v_cach
  * int32): cache length before the new token.  splits >= 1: the keys are split across that
  * many CTAs per (b, h) and merged by log-sum-exp in split order (library-owned scratch).
  * y (dev, dtype): B x (hs*n_head); y_lo (dev, bf16) or NULL receives y - bf16(y).
- * bf16 with head_size 64, splits <= 8 and B * n_head <= 512 streams each (b, h)'s cache rows
- * through shared memory with bulk copies, whole stages of 64 keys per split (the decode step's
- * kernel); other shapes use 16-byte register loads.  q, k_cache and v_cache 16-byte aligned. */
+ * bf16 with head_size 64 and either splits = 1 and B * n_head <= 512, or splits <= 8 and
+ * B * n_head <= 32, streams each (b, h)'s cache rows through shared memory with bulk copies,
+ * whole stages of 64 keys per split (the decode step's kernel); other shapes use 16-byte
+ * register loads.  q, k_cache and v_cache 16-byte aligned. */
 int gpt_attention_decode(const void* q, const void* k_cache, const void* v_cache, int32_t dtype, int32_t B,
                          int32_t n_head, int32_t head_size, int32_t block, const int32_t* pos0_dev, int32_t splits,
                          void* y, void* y_lo, void* stream);

@@ -409,6 +409,8 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // Decode attention over a grid of (rows x splits) CTAs: the 8-warp form for small grids, the
 // 4-warp form otherwise (DEC_WIDE_MAX_CTAS).  The choice depends on the shapes only, so every
 // entry point gives the same results for the same inputs.
+constexpr int DB_FEW_PAIRS = 32;  // the streamed decode attention takes splits up to this many (b, h)
+
 unsigned long long g_db_attr_mask[2] = {};  // per paged flag: devices whose smem attribute is set
 std::mutex g_db_mu;
 
@@ -430,10 +432,13 @@ cudaError_t launch_dec_attn(int rows, int splits, cudaStream_t st, const T* q, c
                             const KvLayout& kv, int nh, int block, const int* pos0, const int* pos_rows, float* ws,
                             unsigned int* tickets, T* y, T* y_lo, int C, int* err, bool step = false) {
   if constexpr (std::is_same<T, bf16>::value && HSZ == 64) {
-    // up to DB_MAX_SPLITS splits per (b, h): the cache rows streamed through shared memory;
-    // within a decode step (step) as a programmatic dependent that streams the older rows before
-    // the c_attn kernel that appends the newest one has finished
-    if (splits <= DB_MAX_SPLITS && rows <= DEC_WIDE_MAX_CTAS) {
+    // the cache rows streamed through shared memory -- one split per (b, h) for up to 512 pairs
+    // (a decode chain), or up to DB_MAX_SPLITS splits for a few pairs (B = 1); within a decode
+    // step (step) as a programmatic dependent that streams the older rows before the c_attn
+    // kernel that appends the newest one has finished.  In between (the 350M shape at B = 8,
+    // 128 pairs) the register-load kernel measured faster: 1022 against 1058 / 1095 us per step
+    // with 2 / 3 streamed splits.
+    if ((splits == 1 && rows <= DEC_WIDE_MAX_CTAS) || (splits <= DB_MAX_SPLITS && rows <= DB_FEW_PAIRS)) {
       int dev = 0;
       cudaError_t r = cudaGetDevice(&dev);
       if (r == cudaSuccess) r = db_attr<PAGED>(dev);
@@ -930,11 +935,8 @@ int decode_attn_splits(const gpt_model* m, int B, size_t ws_bytes, size_t n_tick
   const int pairs = B * m->nh;
   int s = cdiv(2 * m->num_sms, pairs);
   s = std::max(1, std::min(s, std::min(32, cdiv(m->block, 16))));
-  // the streamed kernel (bf16, head size 64, at most 512 pairs): the same target of about two
-  // CTAs per SM, at most DB_MAX_SPLITS splits of whole 64-key stages (one CTA per SM was
-  // slower at 128 pairs, the 350M shape at B=8: 1058 against 1022 us per step)
-  if (m->bf16 && m->hs == 64 && pairs <= DEC_WIDE_MAX_CTAS)
-    s = std::max(1, std::min(std::min(DB_MAX_SPLITS, cdiv(2 * m->num_sms, pairs)), cdiv(m->block, DB_KEYS)));
+  // a few pairs (B = 1): at most DB_MAX_SPLITS splits, so that the streamed kernel takes them
+  if (m->bf16 && m->hs == 64 && pairs <= DB_FEW_PAIRS) s = std::min(s, DB_MAX_SPLITS);
   while (s > 1 && static_cast<size_t>(pairs) * s * (m->hs + 2) * sizeof(float) > ws_bytes) --s;
   if (static_cast<size_t>(pairs) > n_tickets) s = 1;
   return s;
