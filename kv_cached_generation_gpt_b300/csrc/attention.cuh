@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(32 * DEC_WARPS) attn_decode_kernel(const T* __
 
 // ------------------------------------------------------------------ decode, streamed through shared memory
 
-// The same decode attention for bf16, head size 64 and one split per (b, h), with the cache
-// rows streamed through shared memory instead of registers: a producer warp issues untiled bulk
+// The same decode attention for bf16 and head size 64 (one split per (b, h), or a few for a
+// few pairs), with the cache rows streamed through shared memory instead of registers: a
+// producer warp issues untiled bulk
 // copies of DB_KEYS consecutive K rows and the matching V rows (2 x 8 KiB) into a ring of
 // DB_STAGES stages, and 8 consumer warps score and accumulate from shared memory.  A CTA then
 // keeps up to 48 KiB of loads in flight however few registers its warps hold, which is what a
