@@ -156,17 +156,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Each thread of the warp reads 8 consecutive 32-bit columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // tcgen05.ld of 16 consecutive columns into raw registers, without waiting.  The registers
 // may be used only after tmem_wait_ld16 on them: that wait names them as operands, so the
 // compiler cannot move a use above it.
@@ -193,10 +182,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// Wait for every tcgen05.ld issued so far by this thread (no register operands: use it only when
-// the loaded registers are read after a later tmem_wait_ld16 or through asm that names them).
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 // Wait for every tcgen05.ld issued so far by this thread; r (and s) are the destination registers.
 __device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16], uint32_t (&s)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
