@@ -72,6 +72,22 @@ def test_decode_attention_bytes_per_launch():
     assert b.decode_attn_bytes(64, 12, 64, 768) == 2 * 64 * 12 * 768 * 64 * 2 + 64 * 12 * 64 * 2 * 3
 
 
+def test_committed_attention_profile_describes_the_kernel_source():
+    """The ncu summary behind the roofline's `traffic` was taken on the committed decode
+    attention source (its recorded hash matches), and its DRAM bytes per launch are the
+    algorithmic bytes of that capture (32 sequences, 12 heads, 768 keys) within 2 %: no
+    re-reads."""
+    import hashlib
+    b = _bench()
+    src = hashlib.sha256(open(b.ATTN_SOURCE, "rb").read()).hexdigest()[:16]
+    text = open(b.ATTN_PROFILE).read()
+    assert f"source_sha256_16: {src}" in text
+    traffic = b.attn_traffic_per_launch()
+    assert traffic is not None
+    algorithmic = b.decode_attn_bytes(32, 12, 64, 768)
+    assert algorithmic <= traffic <= 1.02 * algorithmic
+
+
 def test_cpu_baseline_thread_count_follows_the_blas_limit():
     """cpu_baseline reports the threads numpy's BLAS ran with: a one-thread limit on the BLAS
     pools (numpy's and scipy's, loaded with the oracle) reads back as 1, whatever other thread
